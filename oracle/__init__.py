@@ -1,0 +1,190 @@
+"""CPU oracle for fine-grained FP8 quantization and the block-scaled FP8 GEMM.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package.  It is a thin
+numpy/ctypes wrapper over ``fp8fg_oracle.c`` (plain C, single-threaded, FP64 for
+the GEMMs) and shares no code with the CUDA path.
+
+Every array here is a numpy array.  bf16 tensors are passed as their uint16 bit
+patterns, FP8 codes as uint8 (OCP E4M3), scales as float32.  The layouts are
+the plain logical ones:
+
+* ``quant_act_1x128(x[M,K]) -> (q[M,K], s[M,K/128])``
+  (DeepSeek-V3 FP8 excerpt, sunipension.com post 314414, Figure 7(a))
+* ``quant_w_128x128(w[K,N]) -> (q[K,N], s[K/128,N/128])`` (same figure)
+* ``requant_1x128_to_128x1(q[M,K], s[M,K/128]) -> (qT[K,M], sT[K,M/128])``
+  (same page: 1x128 tiles become 128x1 tiles for the backward pass)
+* ``gemm_blockscaled(A[M,K], sA[M,K/128], Bt[N,K], sB, sb_kind) -> C[M,N] float64``
+  (why-be.why-be.co.kr post 55081, Figure 7(b): FP32 promotion of partials
+  per 128-wide K interval, with the two scales applied there)
+* ``grouped_gemm_blockscaled(A, sA, B[G,N,K], sB[G,K/128,N/128], offsets) -> C``
+  (xn--jj0bz6z98ct0a29q.com post 362465: MoE activations dispatched in FP8)
+
+Readings of the pages (format E4M3, scale = amax/448 as one fp32 division,
+codes by round-to-nearest-even of the fp32 quotient, zero groups give s = 0,
+requantization dequantizes with one fp32 multiply) are listed in the C file.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+SB_BLOCK128x128 = 0
+SB_COL128x1 = 1
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        lib.orc_e4m3_decode.restype = ctypes.c_double
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_quant_act_1x128.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+        lib.orc_quant_w_128x128.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+        lib.orc_requant_1x128_to_128x1.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
+        lib.orc_gemm_blockscaled.argtypes = [vp, i64, vp, vp, i64, vp, i32, i64, i64, i64, vp]
+        lib.orc_gemm_blockscaled_sample.argtypes = [vp, i64, vp, vp, i64, vp, i32, i64, i64,
+                                                    i64, vp, vp, i64, vp]
+        lib.orc_grouped_gemm_blockscaled.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64, i64,
+                                                     i64, vp]
+        lib.orc_grouped_gemm_blockscaled_sample.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64,
+                                                            i64, i64, vp, vp, i64, vp]
+        for name in ("orc_quant_act_1x128", "orc_quant_w_128x128",
+                     "orc_requant_1x128_to_128x1", "orc_gemm_blockscaled",
+                     "orc_gemm_blockscaled_sample", "orc_grouped_gemm_blockscaled",
+                     "orc_grouped_gemm_blockscaled_sample"):
+            getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _p(a):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError("oracle %s rejected its arguments (rc=%d)" % (what, rc))
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one E4M3 code (NaN for 0x7F / 0xFF)."""
+    return _load().orc_e4m3_decode(int(code) & 0xFF)
+
+
+def e4m3_encode(y: float) -> int:
+    """Round-to-nearest-even, saturating E4M3 code of one fp32 value."""
+    return int(_load().orc_e4m3_encode(float(np.float32(y))))
+
+
+def e4m3_encode_array(y) -> np.ndarray:
+    """Elementwise ``e4m3_encode`` over a float32 array (slow: one C call each)."""
+    y = np.asarray(y, dtype=np.float32).ravel()
+    lib = _load()
+    return np.fromiter((lib.orc_e4m3_encode(float(v)) for v in y), dtype=np.uint8,
+                       count=y.size)
+
+
+def quant_act_1x128(x):
+    """x: uint16 bf16 bits [M, K] -> (q uint8 [M, K], s float32 [M, K/128])."""
+    x = _c(x, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((M, K // 128), np.float32)
+    _check(_load().orc_quant_act_1x128(_p(x), M, K, K, _p(q), K, _p(s)), "quant_act_1x128")
+    return q, s
+
+
+def quant_w_128x128(w):
+    """w: uint16 bf16 bits [K, N] -> (q uint8 [K, N], s float32 [K/128, N/128])."""
+    w = _c(w, np.uint16)
+    K, N = w.shape
+    q = np.empty((K, N), np.uint8)
+    s = np.empty((K // 128, N // 128), np.float32)
+    _check(_load().orc_quant_w_128x128(_p(w), K, N, N, _p(q), N, _p(s)), "quant_w_128x128")
+    return q, s
+
+
+def requant_1x128_to_128x1(q, s):
+    """(q uint8 [M, K], s float32 [M, K/128]) -> (qT uint8 [K, M], sT float32 [K, M/128])."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    M, K = q.shape
+    assert s.shape == (M, K // 128)
+    qT = np.empty((K, M), np.uint8)
+    sT = np.empty((K, M // 128), np.float32)
+    _check(_load().orc_requant_1x128_to_128x1(_p(q), _p(s), M, K, K, _p(qT), M, _p(sT)),
+           "requant_1x128_to_128x1")
+    return qT, sT
+
+
+def gemm_blockscaled(A, sA, Bt, sB, sb_kind=SB_BLOCK128x128):
+    """Full FP64 block-scaled GEMM.
+
+    A uint8 [M, K], sA float32 [M, K/128]; Bt uint8 [N, K] (B stored K-major);
+    sB float32 [K/128, ceil(N/128)] (block) or [K/128, N] (per column).
+    Returns float64 [M, N]."""
+    A, sA, Bt, sB = _c(A, np.uint8), _c(sA, np.float32), _c(Bt, np.uint8), _c(sB, np.float32)
+    M, K = A.shape
+    N = Bt.shape[0]
+    assert Bt.shape == (N, K) and sA.shape == (M, K // 128)
+    C = np.empty((M, N), np.float64)
+    _check(_load().orc_gemm_blockscaled(_p(A), K, _p(sA), _p(Bt), K, _p(sB), sb_kind,
+                                        M, N, K, _p(C)), "gemm_blockscaled")
+    return C
+
+
+def gemm_blockscaled_sample(A, sA, Bt, sB, sb_kind, ms, ns):
+    """The FP64 GEMM evaluated only at the positions (ms[i], ns[i])."""
+    A, sA, Bt, sB = _c(A, np.uint8), _c(sA, np.float32), _c(Bt, np.uint8), _c(sB, np.float32)
+    ms, ns = _c(ms, np.int64), _c(ns, np.int64)
+    M, K = A.shape
+    N = Bt.shape[0]
+    out = np.empty(ms.size, np.float64)
+    _check(_load().orc_gemm_blockscaled_sample(_p(A), K, _p(sA), _p(Bt), K, _p(sB), sb_kind,
+                                               M, N, K, _p(ms), _p(ns), ms.size, _p(out)),
+           "gemm_blockscaled_sample")
+    return out
+
+
+def grouped_gemm_blockscaled(A, sA, B, sB, offsets):
+    """Grouped FP64 GEMM.  A uint8 [M_total, K]; sA float32 [M_total, K/128];
+    B uint8 [G, N, K]; sB float32 [G, K/128, N/128]; offsets int32 [G+1].
+    Rows outside every expert come back as NaN."""
+    A, sA, B, sB = _c(A, np.uint8), _c(sA, np.float32), _c(B, np.uint8), _c(sB, np.float32)
+    offsets = _c(offsets, np.int32)
+    M_total, K = A.shape
+    G, N, _ = B.shape
+    C = np.full((M_total, N), np.nan, np.float64)
+    _check(_load().orc_grouped_gemm_blockscaled(_p(A), K, _p(sA), _p(B), _p(sB), _p(offsets),
+                                                G, M_total, N, K, _p(C)),
+           "grouped_gemm_blockscaled")
+    return C
+
+
+def grouped_gemm_blockscaled_sample(A, sA, B, sB, offsets, ms, ns):
+    """The grouped GEMM evaluated only at (ms[i], ns[i])."""
+    A, sA, B, sB = _c(A, np.uint8), _c(sA, np.float32), _c(B, np.uint8), _c(sB, np.float32)
+    offsets = _c(offsets, np.int32)
+    ms, ns = _c(ms, np.int64), _c(ns, np.int64)
+    M_total, K = A.shape
+    G, N, _ = B.shape
+    out = np.empty(ms.size, np.float64)
+    _check(_load().orc_grouped_gemm_blockscaled_sample(_p(A), K, _p(sA), _p(B), _p(sB),
+                                                       _p(offsets), G, M_total, N, K,
+                                                       _p(ms), _p(ns), ms.size, _p(out)),
+           "grouped_gemm_blockscaled_sample")
+    return out
