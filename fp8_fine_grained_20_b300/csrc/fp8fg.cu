@@ -1,0 +1,309 @@
+// fp8fg.cu -- the C ABI of libfp8fg.so (declared in include/fp8fg.h):
+// argument validation, tensor-map encoding and kernel launches on the
+// caller's stream.  The library allocates no device memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fp8fg.h"
+#include "gemm.cuh"
+#include "quant.cuh"
+
+namespace {
+
+using namespace fp8fg;
+
+constexpr int kMaxDevices = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    return dev;
+}
+
+int sm_count(int dev) {
+    static int cache[kMaxDevices] = {0};
+    if (dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+fp8_status_t launch_status() {
+    return cudaGetLastError() == cudaSuccess ? FP8_OK : FP8_ERR_CUDA;
+}
+
+// Resident CTAs per SM of a kernel (cached per device).
+template <typename K>
+int blocks_per_sm(K kernel, int threads, int dev, int* cache) {
+    if (dev < 0 || dev >= kMaxDevices) return 1;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess || n < 1) n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// -------------------------------------------------------- tensor maps ----
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major [rows][cols] uint8 matrix (row stride ld bytes) read in boxes of
+// box_rows x 128 bytes with 128-byte swizzling; rows beyond `rows` read as 0.
+bool make_kmajor_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <int SBK, bool GROUPED>
+fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const uint8_t* B, int64_t ldb,
+                         int64_t b_rows, const gemm::Args& args, cudaStream_t stream) {
+    static int attr_set[kMaxDevices] = {0};
+    const int dev = current_device();
+    if (dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    auto kernel = gemm::k_gemm_blockscaled<SBK, GROUPED>;
+    const size_t smem = GROUPED ? gemm::SMEM_GROUPED : gemm::SMEM_PLAIN;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
+            return FP8_ERR_DEVICE;
+        attr_set[dev] = 1;
+    }
+    CUtensorMap tmA, tmB;
+    if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
+    if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BN)) return FP8_ERR_CUDA;
+    const int64_t tiles = static_cast<int64_t>(args.m_blocks) * args.n_blocks;
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    kernel<<<grid, gemm::THREADS, smem, stream>>>(tmA, tmB, args);
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+int fp8fg_version(void) { return 100; }
+
+const char* fp8_status_string(fp8_status_t s) {
+    switch (s) {
+        case FP8_OK: return "FP8_OK";
+        case FP8_ERR_NULL: return "FP8_ERR_NULL: a required pointer is NULL";
+        case FP8_ERR_ALIGN: return "FP8_ERR_ALIGN: pointer not 16-byte aligned or stride not a multiple of 16 bytes";
+        case FP8_ERR_SHAPE: return "FP8_ERR_SHAPE: size negative, too large, or not a multiple of 128 where required";
+        case FP8_ERR_CUDA: return "FP8_ERR_CUDA: a CUDA call failed";
+        case FP8_ERR_DEVICE_TIMEOUT: return "FP8_ERR_DEVICE_TIMEOUT: a bounded device wait gave up";
+        case FP8_ERR_ARG: return "FP8_ERR_ARG: invalid enum or stride argument";
+        case FP8_ERR_DEVICE: return "FP8_ERR_DEVICE: unsupported device or resource limit";
+        case FP8_ERR_DEVICE_GROUPS: return "FP8_ERR_DEVICE_GROUPS: invalid group offsets seen on the device";
+    }
+    return "unknown fp8fg status";
+}
+
+fp8_status_t fp8_get_device_status(void* stream, int32_t* out, int reset) {
+    if (!out) return FP8_ERR_NULL;
+    if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return FP8_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, fp8fg::g_fp8_device_status, sizeof(int)) != cudaSuccess) return FP8_ERR_CUDA;
+    *out = v;
+    if (reset) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(fp8fg::g_fp8_device_status, &zero, sizeof(int)) != cudaSuccess) return FP8_ERR_CUDA;
+    }
+    return FP8_OK;
+}
+
+fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                 float* s, int64_t s_stride_m, int64_t s_stride_kb, void* stream) {
+    if (M < 0 || K < 0 || K % 128) return FP8_ERR_SHAPE;
+    if (M == 0 || K == 0) return FP8_OK;
+    if (!x || !q || !s) return FP8_ERR_NULL;
+    if (ldx < K || ldq < K || s_stride_m < 0 || s_stride_kb < 0) return FP8_ERR_ARG;
+    if (!aligned16(x) || !aligned16(q) || (ldx * 2) % 16 || ldq % 16 || (reinterpret_cast<uintptr_t>(s) & 3u))
+        return FP8_ERR_ALIGN;
+    const int64_t KB = K / 128;
+    if (M > INT32_MAX || M * KB > (int64_t(1) << 40)) return FP8_ERR_SHAPE;
+    static int occ[kMaxDevices] = {0};
+    const int dev = current_device();
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    constexpr int UNROLL = 4;
+    auto kernel = k_quant_act_1x128<UNROLL>;
+    const int per_sm = blocks_per_sm(kernel, 256, dev, occ);
+    const int64_t pairs = (M * KB + 1) / 2;
+    const int64_t want = ceil_div(pairs, 8 * UNROLL);  // 8 warps per CTA, UNROLL pairs each
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    kernel<<<grid, 256, 0, as_stream(stream)>>>(x, static_cast<int>(M), static_cast<int>(KB), ldx, q, ldq, s,
+                                               s_stride_m, s_stride_kb);
+    return launch_status();
+}
+
+fp8_status_t fp8_quant_w_128x128(const uint16_t* w, int64_t K, int64_t N, int64_t ldw, uint8_t* q, int64_t ldq,
+                                 int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb, void* stream) {
+    if (K < 0 || N < 0 || K % 128 || N % 128) return FP8_ERR_SHAPE;
+    if (q_layout != FP8_KMAJOR_NK && q_layout != FP8_ROWMAJOR_KN) return FP8_ERR_ARG;
+    if (K == 0 || N == 0) return FP8_OK;
+    if (!w || !q || !s) return FP8_ERR_NULL;
+    const int64_t q_min_ld = (q_layout == FP8_KMAJOR_NK) ? K : N;
+    if (ldw < N || ldq < q_min_ld || s_stride_kb < 0 || s_stride_nb < 0) return FP8_ERR_ARG;
+    if (!aligned16(w) || !aligned16(q) || (ldw * 2) % 16 || ldq % 16 || (reinterpret_cast<uintptr_t>(s) & 3u))
+        return FP8_ERR_ALIGN;
+    const int64_t KB = K / 128, NB = N / 128;
+    if (KB * NB > INT32_MAX) return FP8_ERR_SHAPE;
+    static int occ[kMaxDevices] = {0};
+    const int dev = current_device();
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    const int per_sm = blocks_per_sm(k_quant_w_128x128, 256, dev, occ);
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    const int grid = static_cast<int>(KB * NB < cap ? KB * NB : cap);
+    k_quant_w_128x128<<<grid, 256, 0, as_stream(stream)>>>(w, static_cast<int>(KB), static_cast<int>(NB), ldw, q,
+                                                            ldq, q_layout == FP8_KMAJOR_NK ? 1 : 0, s,
+                                                            s_stride_kb, s_stride_nb);
+    return launch_status();
+}
+
+fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, int64_t ldq, const float* s,
+                                        int64_t s_stride_m, int64_t s_stride_kb, uint8_t* qT, int64_t ldqT,
+                                        float* sT, int64_t sT_stride_k, int64_t sT_stride_mb, void* stream) {
+    if (M < 0 || K < 0 || M % 128 || K % 128) return FP8_ERR_SHAPE;
+    if (M == 0 || K == 0) return FP8_OK;
+    if (!q || !s || !qT || !sT) return FP8_ERR_NULL;
+    if (ldq < K || ldqT < M || s_stride_m < 0 || s_stride_kb < 0 || sT_stride_k < 0 || sT_stride_mb < 0)
+        return FP8_ERR_ARG;
+    if (!aligned16(q) || !aligned16(qT) || ldq % 16 || ldqT % 16 || (reinterpret_cast<uintptr_t>(s) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sT) & 3u))
+        return FP8_ERR_ALIGN;
+    const int64_t MB = M / 128, KB = K / 128;
+    if (MB * KB > INT32_MAX) return FP8_ERR_SHAPE;
+    static int occ[kMaxDevices] = {0};
+    const int dev = current_device();
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    const int per_sm = blocks_per_sm(k_requant_1x128_to_128x1, 256, dev, occ);
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    const int grid = static_cast<int>(MB * KB < cap ? MB * KB : cap);
+    k_requant_1x128_to_128x1<<<grid, 256, 0, as_stream(stream)>>>(q, static_cast<int>(MB), static_cast<int>(KB),
+                                                                   ldq, s, s_stride_m, s_stride_kb, qT, ldqT, sT,
+                                                                   sT_stride_k, sT_stride_mb);
+    return launch_status();
+}
+
+fp8_status_t fp8_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
+                                  int64_t sa_stride_kb, const uint8_t* B, int64_t ldb, const float* sB,
+                                  int64_t sb_stride_kb, int64_t sb_stride_n, int sb_kind, uint16_t* C, int64_t ldc,
+                                  int64_t M, int64_t N, int64_t K, void* stream) {
+    if (sb_kind != FP8_SB_BLOCK128x128 && sb_kind != FP8_SB_COL128x1) return FP8_ERR_ARG;
+    if (M < 0 || N < 0 || K < 0 || M % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
+    if (M == 0 || N == 0) return FP8_OK;
+    if (K == 0) return FP8_ERR_SHAPE;
+    if (!A || !sA || !B || !sB || !C) return FP8_ERR_NULL;
+    if (lda < K || ldb < K || ldc < N || sa_stride_m < 0 || sa_stride_kb < 0 || sb_stride_kb < 0 ||
+        sb_stride_n < 0)
+        return FP8_ERR_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 16 || ldb % 16 || (ldc * 2) % 16 ||
+        (reinterpret_cast<uintptr_t>(sA) & 3u) || (reinterpret_cast<uintptr_t>(sB) & 3u))
+        return FP8_ERR_ALIGN;
+    if (M / 128 * ceil_div(N, gemm::BN) > INT32_MAX || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
+        return FP8_ERR_SHAPE;
+    gemm::Args a{};
+    a.sA = sA;
+    a.sa_sm = sa_stride_m;
+    a.sa_skb = sa_stride_kb;
+    a.sB = sB;
+    a.sb_skb = sb_stride_kb;
+    a.sb_sn = sb_stride_n;
+    a.sb_group_stride = 0;
+    a.C = C;
+    a.ldc = ldc;
+    a.M = static_cast<int>(M);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.m_blocks = static_cast<int>(M / gemm::BM);
+    a.n_blocks = static_cast<int>(ceil_div(N, gemm::BN));
+    a.k_blocks = static_cast<int>(K / gemm::BK);
+    a.sb_cols = static_cast<int>(sb_kind == FP8_SB_COL128x1 ? N : N / 128);
+    a.offsets = nullptr;
+    a.G = 0;
+    if (sb_kind == FP8_SB_COL128x1)
+        return launch_gemm<gemm::SB_COL, false>(A, lda, M, B, ldb, N, a, as_stream(stream));
+    return launch_gemm<gemm::SB_BLOCK, false>(A, lda, M, B, ldb, N, a, as_stream(stream));
+}
+
+fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
+                                          int64_t sa_stride_kb, const uint8_t* B, const float* sB,
+                                          const int32_t* d_group_offsets, int G, int64_t M_total, int64_t N,
+                                          int64_t K, uint16_t* C, int64_t ldc, void* stream) {
+    if (G < 1 || G > gemm::MAX_GROUPS) return FP8_ERR_ARG;
+    if (M_total < 0 || N < 0 || K < 0 || M_total % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
+    if (M_total == 0 || N == 0) return FP8_OK;
+    if (K == 0) return FP8_ERR_SHAPE;
+    if (!A || !sA || !B || !sB || !C || !d_group_offsets) return FP8_ERR_NULL;
+    if (lda < K || ldc < N || sa_stride_m < 0 || sa_stride_kb < 0) return FP8_ERR_ARG;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 16 || (ldc * 2) % 16 ||
+        (reinterpret_cast<uintptr_t>(sA) & 3u) || (reinterpret_cast<uintptr_t>(sB) & 3u) ||
+        (reinterpret_cast<uintptr_t>(d_group_offsets) & 3u))
+        return FP8_ERR_ALIGN;
+    if (static_cast<int64_t>(G) * N > INT32_MAX || M_total > INT32_MAX || K > INT32_MAX ||
+        M_total / 128 * ceil_div(N, gemm::BN) > INT32_MAX)
+        return FP8_ERR_SHAPE;
+    const int64_t KB = K / 128, NB = N / 128;
+    gemm::Args a{};
+    a.sA = sA;
+    a.sa_sm = sa_stride_m;
+    a.sa_skb = sa_stride_kb;
+    a.sB = sB;
+    a.sb_skb = NB;
+    a.sb_sn = 1;
+    a.sb_group_stride = KB * NB;
+    a.C = C;
+    a.ldc = ldc;
+    a.M = static_cast<int>(M_total);
+    a.N = static_cast<int>(N);
+    a.K = static_cast<int>(K);
+    a.m_blocks = static_cast<int>(M_total / gemm::BM);
+    a.n_blocks = static_cast<int>(ceil_div(N, gemm::BN));
+    a.k_blocks = static_cast<int>(KB);
+    a.sb_cols = static_cast<int>(NB);
+    a.offsets = d_group_offsets;
+    a.G = G;
+    return launch_gemm<gemm::SB_BLOCK, true>(A, lda, M_total, B, K, static_cast<int64_t>(G) * N, a,
+                                             as_stream(stream));
+}
+
+}  // extern "C"

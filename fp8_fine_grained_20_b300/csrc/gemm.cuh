@@ -1,0 +1,418 @@
+// gemm.cuh -- block-scaled FP8 GEMM with FP32 promotion every 128 K, for
+// sm_103a (tcgen05 + TMA + TMEM), in three flavours selected at compile time:
+// forward (1x128 A scales x 128x128 B scales), weight gradient (1x128-along-K
+// scales on both operands, i.e. a per-column B scale) and grouped (MoE
+// experts, forward flavour per expert).
+//
+// Method (DeepSeek-V3 FP8 excerpts): tensor cores accumulate a K-interval with
+// limited precision; at the end of the interval the partial sums are copied
+// to FP32 registers on CUDA cores, multiplied by the two group scales and
+// accumulated in full FP32 (why-be.why-be.co.kr post 55081, Figure 7(b);
+// xn--jj0bz6z98ct0a29q.com post 362465).  The interval here is the 128-wide
+// quantization group, so each promotion applies exactly one (sA, sB) pair.
+//
+// B300 design (not the H800 one, where two WGMMA warpgroups alternate
+// between MMA and promotion):
+//   * persistent CTAs (one per SM), 128 x 256 output tiles, grouped raster;
+//   * warp 0: TMA producer -- A (128x128 B) and B (256x128 B) boxes with
+//     128-byte swizzle into a 4-stage shared-memory ring;
+//   * warp 1: MMA issuer -- per K-block, 4 x tcgen05.mma.kind::f8f6f4
+//     (128x256x32) into one of two TMEM partial buffers (2 x 256 columns),
+//     then tcgen05.commit to free the smem stage and publish the partial;
+//   * warp 2: scale loader -- cp.async of the K-block's sA[128] and sB slice
+//     into an 8-slot ring (any scale strides);
+//   * warps 4-11: promotion -- tcgen05.ld of the partial (each warp: its
+//     32 TMEM lanes = rows, one 128-column half), release of the TMEM buffer,
+//     acc += partial * sA * sB in FP32 registers, bf16 store at tile end.
+//   The MMA of K-block kb+1 runs while K-block kb is promoted.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace fp8fg {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;
+constexpr int STAGES = 4;
+constexpr int SSLOTS = 8;
+constexpr int THREADS = 384;
+constexpr int GROUP_M = 16;
+constexpr int MAX_GROUPS = 1024;
+constexpr uint32_t A_BYTES = BM * BK;
+constexpr uint32_t B_BYTES = BN * BK;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+
+constexpr int SB_BLOCK = 0;  // sB[kb][n/128]
+constexpr int SB_COL = 1;    // sB[kb][n]
+
+constexpr size_t OFF_A = 0;
+constexpr size_t OFF_B = OFF_A + STAGES * A_BYTES;
+constexpr size_t OFF_SA = OFF_B + STAGES * B_BYTES;
+constexpr size_t OFF_SB = OFF_SA + SSLOTS * BM * sizeof(float);
+constexpr size_t OFF_BAR = OFF_SB + SSLOTS * BN * sizeof(float);
+constexpr int N_BARS = 2 * STAGES + 4 + 2 * SSLOTS + 1;
+constexpr size_t OFF_MISC = OFF_BAR + N_BARS * sizeof(uint64_t);
+constexpr size_t OFF_GOFF = OFF_MISC + 16;
+constexpr size_t SMEM_PLAIN = 1024 + OFF_GOFF;
+constexpr size_t SMEM_GROUPED = 1024 + OFF_GOFF + (MAX_GROUPS + 1) * sizeof(int);
+
+struct Args {
+    const float* sA;
+    int64_t sa_sm, sa_skb;
+    const float* sB;
+    int64_t sb_skb, sb_sn;
+    int64_t sb_group_stride;  // grouped: floats between experts' scale tables
+    uint16_t* C;
+    int64_t ldc;
+    int M, N, K;
+    int m_blocks, n_blocks, k_blocks;
+    int sb_cols;              // number of valid sB columns: N/128 (block) or N (per column)
+    const int32_t* offsets;   // grouped only (device)
+    int G;
+};
+
+__device__ const float g_zero_scale = 0.0f;
+
+// Tile t -> (m-block, n-block): GROUP_M consecutive m-blocks share each
+// n-block before moving on, so concurrently running CTAs reuse A and B in L2.
+__device__ __forceinline__ void tile_coords(int t, const Args& p, int& mb, int& nb) {
+    const int span = GROUP_M * p.n_blocks;
+    const int grp = t / span;
+    const int first = grp * GROUP_M;
+    const int gm = min(GROUP_M, p.m_blocks - first);
+    const int r = t - grp * span;
+    mb = first + r % gm;
+    nb = r / gm;
+}
+
+// Expert owning the 128-row block mb, or -1 (rows beyond the last expert).
+__device__ __forceinline__ int expert_of_block(int mb, const int* goff, int G) {
+    const int row = mb * BM;
+    if (row >= goff[G]) return -1;
+    int lo = 0, hi = G - 1;  // largest g with goff[g] <= row
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (goff[mid] <= row) lo = mid; else hi = mid - 1;
+    }
+    return (row >= goff[lo] && row < goff[lo + 1]) ? lo : -1;
+}
+
+template <bool GROUPED>
+__device__ __forceinline__ bool tile_info(int t, const Args& p, const int* goff, int& mb, int& nb, int& g) {
+    tile_coords(t, p, mb, nb);
+    if (!GROUPED) {
+        g = 0;
+        return true;
+    }
+    g = expert_of_block(mb, goff, p.G);
+    return g >= 0;
+}
+
+__device__ __forceinline__ void signal_abort(volatile int* abort_flag) {
+    *abort_flag = 1;
+    record_status(kStatusTimeout);
+}
+
+template <int SBK, int OFF>
+__device__ __forceinline__ void promote32(float (&acc)[128], const uint32_t (&r)[32], float sc, float sa,
+                                          const float* sbv) {
+    if (SBK == SB_BLOCK) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[OFF + j] = fmaf(__uint_as_float(r[j]), sc, acc[OFF + j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 b = *reinterpret_cast<const float4*>(sbv + OFF + j);
+            acc[OFF + j + 0] = fmaf(__uint_as_float(r[j + 0]), __fmul_rn(sa, b.x), acc[OFF + j + 0]);
+            acc[OFF + j + 1] = fmaf(__uint_as_float(r[j + 1]), __fmul_rn(sa, b.y), acc[OFF + j + 1]);
+            acc[OFF + j + 2] = fmaf(__uint_as_float(r[j + 2]), __fmul_rn(sa, b.z), acc[OFF + j + 2]);
+            acc[OFF + j + 3] = fmaf(__uint_as_float(r[j + 3]), __fmul_rn(sa, b.w), acc[OFF + j + 3]);
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int SBK, bool GROUPED>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_blockscaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const Args p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sm_a = base + OFF_A;
+    uint8_t* sm_b = base + OFF_B;
+    float* sm_sa = reinterpret_cast<float*>(base + OFF_SA);
+    float* sm_sb = reinterpret_cast<float*>(base + OFF_SB);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + OFF_BAR);
+    uint64_t* full = bars;
+    uint64_t* empty = full + STAGES;
+    uint64_t* tfull = empty + STAGES;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* sfull = tempty + 2;
+    uint64_t* sempty = sfull + SSLOTS;
+    uint64_t* drain = sempty + SSLOTS;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + OFF_MISC + 4);
+    int* groups_ok = reinterpret_cast<int*>(base + OFF_MISC + 8);
+    int* goff = reinterpret_cast<int*>(base + OFF_GOFF);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tfull[i], 1);
+            mbar_init(&tempty[i], 8);
+        }
+        for (int i = 0; i < SSLOTS; ++i) {
+            mbar_init(&sfull[i], 32);
+            mbar_init(&sempty[i], 8);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *groups_ok = 1;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (GROUPED) {
+        for (int i = threadIdx.x; i <= p.G; i += THREADS) goff[i] = p.offsets[i];
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (GROUPED && threadIdx.x == 0) {
+        bool ok = goff[0] >= 0 && goff[p.G] <= p.M;
+        for (int g = 0; g < p.G; ++g) ok = ok && goff[g] <= goff[g + 1] && (goff[g] % BM) == 0;
+        ok = ok && (goff[p.G] % BM) == 0;
+        if (!ok) {
+            *groups_ok = 0;
+            if (blockIdx.x == 0) record_status(kStatusBadGroups);
+        }
+    }
+    __syncthreads();
+    const uint32_t tmem = *tmem_slot;
+    const int num_tiles = (*groups_ok) ? p.m_blocks * p.n_blocks : 0;
+
+    if (warp < 4) {
+      regs_decrease<40>();
+      if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                int mb, nb, g;
+                if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
+                const int a_y = mb * BM;
+                const int b_y = g * p.N + nb * BN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                        signal_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
+                    tma_load_2d(sm_a + stage * A_BYTES, &tmA, &full[stage], kb * BK, a_y);
+                    tma_load_2d(sm_b + stage * B_BYTES, &tmB, &full[stage], kb * BK, b_y);
+                    ++issued;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // drain the loads still in flight before the CTA may exit
+                const uint32_t n = issued < STAGES ? issued : STAGES;
+                for (uint32_t i = 1; i <= n; ++i) {
+                    const uint32_t k = issued - i;
+                    mbar_wait(&full[k % STAGES], (k / STAGES) & 1u, nullptr, kDrainTimeoutNs);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                int mb, nb, g;
+                if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    const uint32_t buf = it & 1u;
+                    const uint32_t tph = (it >> 1) & 1u;
+                    if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag) ||
+                        !mbar_wait(&full[stage], phase, abort_flag)) {
+                        signal_abort(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d = tmem + buf * BN;
+                    const uint64_t ad = sdesc_kmajor_sw128(smem_addr(sm_a + stage * A_BYTES));
+                    const uint64_t bd = sdesc_kmajor_sw128(smem_addr(sm_b + stage * B_BYTES));
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k) {
+                        // +32 bytes along K inside the 128-byte swizzle atom: +2 in the (>>4) address field
+                        umma_f8(d, ad + 2u * k, bd + 2u * k, IDESC, k > 0 ? 1u : 0u);
+                    }
+                    umma_commit(&empty[stage]);
+                    umma_commit(&tfull[buf]);
+                    ++it;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every MMA this thread issued completes before TMEM is released
+            umma_commit(drain);
+            mbar_wait(drain, 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ scale loader ----
+        uint32_t slot = 0, sph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            int mb, nb, g;
+            if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
+            const float* sa_rows = p.sA + static_cast<int64_t>(mb) * BM * p.sa_sm;
+            const float* sb_base = p.sB + static_cast<int64_t>(g) * p.sb_group_stride;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sempty[slot], sph ^ 1u, abort_flag))) {
+                    if (lane == 0) signal_abort(abort_flag);
+                    ok = false;
+                    break;
+                }
+                float* dsa = sm_sa + slot * BM;
+#pragma unroll
+                for (int i = 0; i < BM / 32; ++i) {
+                    const int r = lane + 32 * i;
+                    cp_async_4(dsa + r, sa_rows + static_cast<int64_t>(r) * p.sa_sm +
+                                            static_cast<int64_t>(kb) * p.sa_skb);
+                }
+                float* dsb = sm_sb + slot * BN;
+                if (SBK == SB_BLOCK) {
+                    if (lane < BN / 128) {
+                        const int c = nb * (BN / 128) + lane;
+                        const float* src = (c < p.sb_cols) ? sb_base + static_cast<int64_t>(kb) * p.sb_skb +
+                                                                 static_cast<int64_t>(c) * p.sb_sn
+                                                           : &g_zero_scale;
+                        cp_async_4(dsb + lane, src);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < BN / 32; ++i) {
+                        const int j = lane + 32 * i;
+                        const int c = nb * BN + j;
+                        const float* src = (c < p.sb_cols) ? sb_base + static_cast<int64_t>(kb) * p.sb_skb +
+                                                                 static_cast<int64_t>(c) * p.sb_sn
+                                                           : &g_zero_scale;
+                        cp_async_4(dsb + j, src);
+                    }
+                }
+                cp_async_arrive_noinc(&sfull[slot]);
+                if (++slot == SSLOTS) {
+                    slot = 0;
+                    sph ^= 1u;
+                }
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+      }
+    } else {
+        regs_increase<232>();
+        // ------------------------------------- promotion and epilogue ----
+        const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+        const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
+        const int row = quarter * 32 + lane;
+        uint32_t it = 0, slot = 0, sph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+            int mb, nb, g;
+            if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
+            float acc[128];
+#pragma unroll
+            for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+            for (int kb = 0; kb < p.k_blocks; ++kb) {
+                const uint32_t buf = it & 1u;
+                const uint32_t tph = (it >> 1) & 1u;
+                const bool ready = mbar_wait(&sfull[slot], sph, abort_flag) && mbar_wait(&tfull[buf], tph, abort_flag);
+                if (!__all_sync(0xffffffffu, ready)) {  // warp-uniform: tcgen05.ld is .sync.aligned
+                    if (lane == 0) signal_abort(abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const float sa = sm_sa[slot * BM + row];
+                const float* sbv = sm_sb + slot * BN + half * 128;
+                const float sc = (SBK == SB_BLOCK) ? __fmul_rn(sa, sm_sb[slot * BN + half]) : 0.0f;
+                const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN + half * 128;
+                uint32_t r0[32], r1[32];
+                tmem_ld_32cols(taddr + 0, r0);
+                tmem_wait_ld(r0);
+                tmem_ld_32cols(taddr + 32, r1);
+                promote32<SBK, 0>(acc, r0, sc, sa, sbv);
+                tmem_wait_ld(r1);
+                tmem_ld_32cols(taddr + 64, r0);
+                promote32<SBK, 32>(acc, r1, sc, sa, sbv);
+                tmem_wait_ld(r0);
+                tmem_ld_32cols(taddr + 96, r1);
+                promote32<SBK, 64>(acc, r0, sc, sa, sbv);
+                tmem_wait_ld(r1);
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[buf]);
+                promote32<SBK, 96>(acc, r1, sc, sa, sbv);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[slot]);
+                ++it;
+                if (++slot == SSLOTS) {
+                    slot = 0;
+                    sph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            const int n0 = nb * BN + half * 128;
+            if (n0 < p.N) {
+                uint16_t* crow = p.C + static_cast<int64_t>(mb * BM + row) * p.ldc + n0;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    uint4 w;
+                    w.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+                    w.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+                    w.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+                    w.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+                    stg_v4(crow + 8 * j, w);
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm
+}  // namespace fp8fg

@@ -1,0 +1,193 @@
+/*
+ * fp8fg.h -- C ABI of libfp8fg.so: fine-grained FP8 quantization and the
+ * block-scaled FP8 GEMM on NVIDIA B300 (sm_103a).
+ *
+ * The method (DeepSeek-V3 FP8 training excerpts; pages named by address):
+ *  - sunipension.com, board post 314414, Figure 7(a): activations are grouped
+ *    and scaled per 1x128 tile (one token, 128 channels), weights per 128x128
+ *    block (128 input x 128 output channels); cached activations are converted
+ *    from 1x128 tiles to 128x1 tiles for the backward pass; Figure 6: the
+ *    weight-gradient (Wgrad) GEMM runs in FP8.
+ *  - why-be.why-be.co.kr, board post 55081, Figure 7(b): tensor-core partial
+ *    sums are copied to FP32 registers on CUDA cores every K-interval and
+ *    accumulated there in full FP32.
+ *  - xn--jj0bz6z98ct0a29q.com, board post 362465: the per-group scales are
+ *    applied during that FP32 promotion; MoE activations are dispatched in FP8.
+ *  - why-be.why-be.co.kr, board post 65900: scaling maps the largest magnitude
+ *    of a group onto the largest FP8 value.
+ *
+ * Numerics (identical on every entry point):
+ *  - FP8 codes are OCP E4M3 ("e4m3fn", max 448) stored as uint8.
+ *  - bf16 tensors are passed as their uint16 bit patterns.
+ *  - For each group: amax = max |x| (fp32), s = amax / 448 (one IEEE fp32
+ *    division, no flush to zero), code = E4M3 round-to-nearest-even, saturating,
+ *    of the fp32 quotient x / s (one IEEE fp32 division); the sign of x is kept
+ *    (a negative x that rounds to zero gives 0x80).  A group with amax == 0
+ *    stores s = 0 and codes 0x00.  Inputs must be finite.
+ *  - The GEMM promotion interval is the 128-wide K group: for every K-block kb
+ *    the tensor-core partial sum of that block is multiplied by
+ *    sA[m,kb] * sB[kb,n] and added to an FP32 accumulator; the output is
+ *    rounded once to bf16 (nearest even).
+ *
+ * Conventions:
+ *  - Every pointer is DEVICE memory owned by the caller; the library allocates
+ *    nothing per call and keeps no pointer after the call returns.
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream) and never synchronises.  Calls on one stream run in order.
+ *  - Argument checks run on the host before anything is launched; a non-OK
+ *    status means nothing was launched.  FP8_ERR_CUDA reports a launch error.
+ *  - Leading dimensions ("ld*") and strides are in ELEMENTS of the pointed-to
+ *    type.  Device pointers must be 16-byte aligned, code/bf16 row strides must
+ *    be multiples of 16 bytes.
+ *  - Scale tensors have a logical shape and two explicit element strides, so
+ *    the MN-major layout (stride 1 along the row/column index, which the GEMM
+ *    reads fastest) and the row-major layout are both accepted.
+ *  - Device-side waits are bounded.  A kernel that gives up sets a bit in a
+ *    library-owned device status word and returns; read it with
+ *    fp8_get_device_status().
+ */
+#ifndef FP8FG_H
+#define FP8FG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fp8_status {
+    FP8_OK = 0,
+    FP8_ERR_NULL = 1,            /* a required pointer is NULL */
+    FP8_ERR_ALIGN = 2,           /* pointer not 16-byte aligned or stride not a multiple of 16 bytes */
+    FP8_ERR_SHAPE = 3,           /* a size is negative, or not a multiple of 128 where required */
+    FP8_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed (launch, attribute, tensor map) */
+    FP8_ERR_DEVICE_TIMEOUT = 5,  /* (device status) a bounded device wait gave up */
+    FP8_ERR_ARG = 6,             /* an enum or stride argument is invalid */
+    FP8_ERR_DEVICE = 7,          /* the current device is not sm_103 / lacks resources */
+    FP8_ERR_DEVICE_GROUPS = 8    /* (device status) group offsets were not valid */
+} fp8_status_t;
+
+/* Layout of the codes written by fp8_quant_w_128x128. */
+enum {
+    FP8_KMAJOR_NK = 0,   /* q[n][k] (q + n*ldq + k): the K-major operand layout of the GEMMs */
+    FP8_ROWMAJOR_KN = 1  /* q[k][n], same layout as the bf16 weight */
+};
+
+/* Granularity of the B-operand scales of fp8_gemm_blockscaled. */
+enum {
+    FP8_SB_BLOCK128x128 = 0, /* one scale per 128 (K) x 128 (N) block: logical sB[K/128][N/128] */
+    FP8_SB_COL128x1 = 1      /* one scale per 128 (K) x 1 (N) column group: logical sB[K/128][N] */
+};
+
+/*
+ * 1x128 activation quantization (Figure 7(a), activations).
+ *   x     bf16 [M][K], row stride ldx (>= K)
+ *   q     E4M3 codes [M][K], row stride ldq (>= K)
+ *   s     fp32 scales, logical [M][K/128]; element (m, kb) at s[m*s_stride_m + kb*s_stride_kb].
+ *         MN-major (the GEMM's preferred operand layout): s_stride_m = 1, s_stride_kb >= M.
+ *         Row-major: s_stride_m = K/128, s_stride_kb = 1.
+ * Requires K % 128 == 0; M may be any value >= 0 (M == 0 launches nothing).
+ */
+fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                 uint8_t* q, int64_t ldq,
+                                 float* s, int64_t s_stride_m, int64_t s_stride_kb,
+                                 void* stream);
+
+/*
+ * 128x128 weight quantization (Figure 7(a), weights).
+ *   w        bf16 [K][N] (K input channels, N output channels), row stride ldw (>= N)
+ *   q        E4M3 codes; q_layout FP8_KMAJOR_NK: q[n][k], row stride ldq (>= K);
+ *            FP8_ROWMAJOR_KN: q[k][n], row stride ldq (>= N)
+ *   s        fp32 scales, logical [K/128][N/128]; (kb, nb) at s[kb*s_stride_kb + nb*s_stride_nb]
+ * Requires K % 128 == 0 and N % 128 == 0.
+ */
+fp8_status_t fp8_quant_w_128x128(const uint16_t* w, int64_t K, int64_t N, int64_t ldw,
+                                 uint8_t* q, int64_t ldq, int q_layout,
+                                 float* s, int64_t s_stride_kb, int64_t s_stride_nb,
+                                 void* stream);
+
+/*
+ * 1x128 -> 128x1 requantization for the backward pass (sunipension.com post
+ * 314414: cached 1x128 activation tiles become 128x1 tiles).  Every value is
+ * dequantized with one fp32 multiply, xhat = decode(q) * s, then every
+ * channel k is quantized in groups of 128 consecutive rows (tokens) and the
+ * result is written transposed.
+ *   q    E4M3 codes [M][K], row stride ldq;  s  logical [M][K/128] at s[m*s_stride_m + kb*s_stride_kb]
+ *   qT   E4M3 codes [K][M], row stride ldqT (>= M)
+ *   sT   logical [K][M/128]; (k, mb) at sT[k*sT_stride_k + mb*sT_stride_mb]
+ *        (for the Wgrad GEMM's operands, MN-major: sT_stride_k = 1, sT_stride_mb >= K)
+ * Requires M % 128 == 0 and K % 128 == 0.
+ */
+fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, int64_t ldq,
+                                        const float* s, int64_t s_stride_m, int64_t s_stride_kb,
+                                        uint8_t* qT, int64_t ldqT,
+                                        float* sT, int64_t sT_stride_k, int64_t sT_stride_mb,
+                                        void* stream);
+
+/*
+ * Block-scaled FP8 GEMM with FP32 promotion every 128 K (Figure 7(b)):
+ *   C[m][n] = bf16( sum_kb sA[m,kb] * sB(kb,n) * sum_{k in kb} A[m][k] * B[n][k] )
+ * with the inner sums on tcgen05 tensor cores and the outer sum in FP32.
+ *   A    E4M3 [M][K] (K contiguous), row stride lda
+ *   sA   logical [M][K/128]; (m, kb) at sA[m*sa_stride_m + kb*sa_stride_kb]
+ *   B    E4M3 [N][K] (K contiguous: the "K-major" / transposed weight), row stride ldb
+ *   sB   sb_kind FP8_SB_BLOCK128x128 (forward, 128x128 weight blocks): logical
+ *        [K/128][N/128], (kb, nb) at sB[kb*sb_stride_kb + nb*sb_stride_n];
+ *        FP8_SB_COL128x1 (weight gradient, both operands 128x1-quantized along
+ *        K): logical [K/128][N], (kb, n) at sB[kb*sb_stride_kb + n*sb_stride_n]
+ *   C    bf16 [M][N], row stride ldc
+ * Requires M % 128 == 0, N % 128 == 0, K % 128 == 0 (M, N or K == 0 launches nothing
+ * when the output is empty; K == 0 with M*N > 0 is FP8_ERR_SHAPE).
+ */
+fp8_status_t fp8_gemm_blockscaled(const uint8_t* A, int64_t lda,
+                                  const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
+                                  const uint8_t* B, int64_t ldb,
+                                  const float* sB, int64_t sb_stride_kb, int64_t sb_stride_n,
+                                  int sb_kind,
+                                  uint16_t* C, int64_t ldc,
+                                  int64_t M, int64_t N, int64_t K,
+                                  void* stream);
+
+/*
+ * Grouped block-scaled FP8 GEMM for a variable-size MoE expert batch
+ * (xn--jj0bz6z98ct0a29q.com post 362465: activations dispatched in FP8).
+ * Expert g owns rows [off[g], off[g+1]) of A and C and multiplies them by B_g:
+ *   C[m][n] = bf16( sum_kb sA[m,kb] * sB[g][kb][n/128] * sum_{k in kb} A[m][k] * B[g][n][k] )
+ *   A               E4M3 [M_total][K], row stride lda;  sA as in fp8_gemm_blockscaled
+ *   B               E4M3 [G][N][K], dense (expert stride N*K)
+ *   sB              fp32 [G][K/128][N/128], dense
+ *   d_group_offsets DEVICE int32 [G+1]; 0 <= off[0] <= ... <= off[G] <= M_total,
+ *                   every entry a multiple of 128.  Read only on the device: the
+ *                   host never synchronises.  Invalid offsets set
+ *                   FP8_ERR_DEVICE_GROUPS in the device status and no tile is computed.
+ *   C               bf16 [M_total][N], row stride ldc; rows outside every expert
+ *                   are not written.
+ * Requires M_total % 128 == 0, N % 128 == 0, K % 128 == 0, 1 <= G <= 1024.
+ */
+fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda,
+                                          const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
+                                          const uint8_t* B, const float* sB,
+                                          const int32_t* d_group_offsets, int G,
+                                          int64_t M_total, int64_t N, int64_t K,
+                                          uint16_t* C, int64_t ldc,
+                                          void* stream);
+
+/*
+ * Device status word.  Waits for `stream`, copies the status word of the
+ * current device into *out (FP8_OK or the first FP8_ERR_DEVICE_* recorded since
+ * the last reset) and, if reset != 0, clears it.  Returns FP8_ERR_CUDA if the
+ * copy fails.
+ */
+fp8_status_t fp8_get_device_status(void* stream, int32_t* out, int reset);
+
+/* Static, human-readable name of a status code. */
+const char* fp8_status_string(fp8_status_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int fp8fg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8FG_H */

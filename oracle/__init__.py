@@ -62,6 +62,7 @@ def _load():
                      "orc_gemm_blockscaled_sample", "orc_grouped_gemm_blockscaled",
                      "orc_grouped_gemm_blockscaled_sample"):
             getattr(lib, name).restype = ctypes.c_int
+        lib.orc_e4m3_decode(0)      # fills the oracle's magnitude table before any threaded call
         _lib = lib
     return _lib
 
@@ -98,36 +99,82 @@ def e4m3_encode_array(y) -> np.ndarray:
                        count=y.size)
 
 
-def quant_act_1x128(x):
-    """x: uint16 bf16 bits [M, K] -> (q uint8 [M, K], s float32 [M, K/128])."""
+def _chunks(n, parts, align):
+    """Split range(n) into at most `parts` pieces whose bounds are multiples of `align`."""
+    units = n // align
+    parts = max(1, min(parts, units)) if units else 1
+    bounds = [align * (units * i // parts) for i in range(parts)] + [n]
+    return [(bounds[i], bounds[i + 1]) for i in range(parts) if bounds[i + 1] > bounds[i]]
+
+
+def _run_parallel(jobs, threads):
+    """Run independent oracle calls; ctypes releases the GIL, so threads run in
+    parallel.  Only the work distribution is parallel: every call is the plain
+    single-threaded C routine on its own rows."""
+    if threads is None or threads <= 1 or len(jobs) <= 1:
+        return [j() for j in jobs]
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(lambda j: j(), jobs))
+
+
+def default_threads():
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def quant_act_1x128(x, threads=None):
+    """x: uint16 bf16 bits [M, K] -> (q uint8 [M, K], s float32 [M, K/128]).
+    `threads` splits the rows (each 1x128 group lies in one row)."""
     x = _c(x, np.uint16)
     M, K = x.shape
     q = np.empty((M, K), np.uint8)
     s = np.empty((M, K // 128), np.float32)
-    _check(_load().orc_quant_act_1x128(_p(x), M, K, K, _p(q), K, _p(s)), "quant_act_1x128")
+    lib = _load()
+
+    def job(r0, r1):
+        return lambda: _check(lib.orc_quant_act_1x128(_p(x[r0:]), r1 - r0, K, K, _p(q[r0:]), K,
+                                                      _p(s[r0:])), "quant_act_1x128")
+    _run_parallel([job(a, b) for a, b in _chunks(M, threads or 1, 1)] if M else [], threads)
     return q, s
 
 
-def quant_w_128x128(w):
-    """w: uint16 bf16 bits [K, N] -> (q uint8 [K, N], s float32 [K/128, N/128])."""
+def quant_w_128x128(w, threads=None):
+    """w: uint16 bf16 bits [K, N] -> (q uint8 [K, N], s float32 [K/128, N/128]).
+    `threads` splits the K rows on 128-row block boundaries."""
     w = _c(w, np.uint16)
     K, N = w.shape
     q = np.empty((K, N), np.uint8)
     s = np.empty((K // 128, N // 128), np.float32)
-    _check(_load().orc_quant_w_128x128(_p(w), K, N, N, _p(q), N, _p(s)), "quant_w_128x128")
+    lib = _load()
+
+    def job(r0, r1):
+        return lambda: _check(lib.orc_quant_w_128x128(_p(w[r0:]), r1 - r0, N, N, _p(q[r0:]), N,
+                                                      _p(s[r0 // 128:])), "quant_w_128x128")
+    if K % 128 or N % 128:
+        _check(-1, "quant_w_128x128")
+    _run_parallel([job(a, b) for a, b in _chunks(K, threads or 1, 128)] if K else [], threads)
     return q, s
 
 
-def requant_1x128_to_128x1(q, s):
-    """(q uint8 [M, K], s float32 [M, K/128]) -> (qT uint8 [K, M], sT float32 [K, M/128])."""
+def requant_1x128_to_128x1(q, s, threads=None):
+    """(q uint8 [M, K], s float32 [M, K/128]) -> (qT uint8 [K, M], sT float32 [K, M/128]).
+    `threads` splits the channels on 128-channel boundaries."""
     q = _c(q, np.uint8)
     s = _c(s, np.float32)
     M, K = q.shape
     assert s.shape == (M, K // 128)
     qT = np.empty((K, M), np.uint8)
     sT = np.empty((K, M // 128), np.float32)
-    _check(_load().orc_requant_1x128_to_128x1(_p(q), _p(s), M, K, K, _p(qT), M, _p(sT)),
-           "requant_1x128_to_128x1")
+    lib = _load()
+    if M % 128 or K % 128:
+        _check(-1, "requant_1x128_to_128x1")
+
+    def job(k0, k1):
+        s_part = np.ascontiguousarray(s[:, k0 // 128:k1 // 128])
+        return lambda: _check(lib.orc_requant_1x128_to_128x1(_p(q[:, k0:]), _p(s_part), M, k1 - k0, K,
+                                                             _p(qT[k0:]), M, _p(sT[k0:])),
+                              "requant_1x128_to_128x1")
+    _run_parallel([job(a, b) for a, b in _chunks(K, threads or 1, 128)] if K and M else [], threads)
     return qT, sT
 
 
@@ -147,16 +194,20 @@ def gemm_blockscaled(A, sA, Bt, sB, sb_kind=SB_BLOCK128x128):
     return C
 
 
-def gemm_blockscaled_sample(A, sA, Bt, sB, sb_kind, ms, ns):
+def gemm_blockscaled_sample(A, sA, Bt, sB, sb_kind, ms, ns, threads=None):
     """The FP64 GEMM evaluated only at the positions (ms[i], ns[i])."""
     A, sA, Bt, sB = _c(A, np.uint8), _c(sA, np.float32), _c(Bt, np.uint8), _c(sB, np.float32)
     ms, ns = _c(ms, np.int64), _c(ns, np.int64)
     M, K = A.shape
     N = Bt.shape[0]
     out = np.empty(ms.size, np.float64)
-    _check(_load().orc_gemm_blockscaled_sample(_p(A), K, _p(sA), _p(Bt), K, _p(sB), sb_kind,
-                                               M, N, K, _p(ms), _p(ns), ms.size, _p(out)),
-           "gemm_blockscaled_sample")
+    lib = _load()
+
+    def job(i0, i1):
+        return lambda: _check(lib.orc_gemm_blockscaled_sample(_p(A), K, _p(sA), _p(Bt), K, _p(sB), sb_kind,
+                                                              M, N, K, _p(ms[i0:]), _p(ns[i0:]), i1 - i0,
+                                                              _p(out[i0:])), "gemm_blockscaled_sample")
+    _run_parallel([job(a, b) for a, b in _chunks(ms.size, threads or 1, 1)] if ms.size else [], threads)
     return out
 
 
@@ -175,7 +226,7 @@ def grouped_gemm_blockscaled(A, sA, B, sB, offsets):
     return C
 
 
-def grouped_gemm_blockscaled_sample(A, sA, B, sB, offsets, ms, ns):
+def grouped_gemm_blockscaled_sample(A, sA, B, sB, offsets, ms, ns, threads=None):
     """The grouped GEMM evaluated only at (ms[i], ns[i])."""
     A, sA, B, sB = _c(A, np.uint8), _c(sA, np.float32), _c(B, np.uint8), _c(sB, np.float32)
     offsets = _c(offsets, np.int32)
@@ -183,8 +234,13 @@ def grouped_gemm_blockscaled_sample(A, sA, B, sB, offsets, ms, ns):
     M_total, K = A.shape
     G, N, _ = B.shape
     out = np.empty(ms.size, np.float64)
-    _check(_load().orc_grouped_gemm_blockscaled_sample(_p(A), K, _p(sA), _p(B), _p(sB),
-                                                       _p(offsets), G, M_total, N, K,
-                                                       _p(ms), _p(ns), ms.size, _p(out)),
-           "grouped_gemm_blockscaled_sample")
+    lib = _load()
+
+    def job(i0, i1):
+        return lambda: _check(lib.orc_grouped_gemm_blockscaled_sample(_p(A), K, _p(sA), _p(B), _p(sB),
+                                                                      _p(offsets), G, M_total, N, K,
+                                                                      _p(ms[i0:]), _p(ns[i0:]), i1 - i0,
+                                                                      _p(out[i0:])),
+                              "grouped_gemm_blockscaled_sample")
+    _run_parallel([job(a, b) for a, b in _chunks(ms.size, threads or 1, 1)] if ms.size else [], threads)
     return out

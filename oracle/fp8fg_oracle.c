@@ -61,14 +61,31 @@ static double e4m3_magnitude(int code)
 }
 
 /* Decode any code to a double (exact); NaN for 0x7F and 0xFF. */
+static const double *magnitudes(void);
+
 double orc_e4m3_decode(uint8_t code)
 {
     int mag = code & 0x7F;
     double v;
     if (mag == 0x7F)
         return NAN;
-    v = e4m3_magnitude(mag);
+    v = magnitudes()[mag];
     return (code & 0x80) ? -v : v;
+}
+
+/* The 127 finite non-negative magnitudes, indexed by code 0x00..0x7E. */
+static double mag_table[0x7F];
+static int mag_table_ready = 0;
+
+static const double *magnitudes(void)
+{
+    int c;
+    if (!mag_table_ready) {
+        for (c = 0; c < 0x7F; ++c)
+            mag_table[c] = e4m3_magnitude(c);
+        mag_table_ready = 1;
+    }
+    return mag_table;
 }
 
 /* Round an fp32 value to the nearest E4M3 code, ties to the even code (the code
@@ -78,6 +95,7 @@ double orc_e4m3_decode(uint8_t code)
  * of the pair, which is exact in double. */
 uint8_t orc_e4m3_encode(float y)
 {
+    const double *mag = magnitudes();
     uint8_t sign = signbit(y) ? 0x80 : 0x00;
     double a = fabs((double)y);
     int lo = 0, hi = 0x7E, c;
@@ -87,14 +105,14 @@ uint8_t orc_e4m3_encode(float y)
         return (uint8_t)(sign | 0x7E);
     while (lo < hi) {           /* largest code with magnitude <= a */
         int t = (lo + hi + 1) / 2;
-        if (e4m3_magnitude(t) <= a)
+        if (mag[t] <= a)
             lo = t;
         else
             hi = t - 1;
     }
-    if (e4m3_magnitude(lo) == a)
+    if (mag[lo] == a)
         return (uint8_t)(sign | lo);
-    mid = 0.5 * (e4m3_magnitude(lo) + e4m3_magnitude(lo + 1));
+    mid = 0.5 * (mag[lo] + mag[lo + 1]);
     if (a < mid)
         c = lo;
     else if (a > mid)

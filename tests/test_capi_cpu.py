@@ -1,0 +1,118 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every
+symbol the header declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_fine_grained_20_b300 as fg
+from fp8_fine_grained_20_b300 import build as fgbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8fg.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fgbuild.build()
+    return fg.capi()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8\w*)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for n in ("fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_requant_1x128_to_128x1",
+              "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in fg._SIGNATURES, name
+
+
+def test_status_strings(lib):
+    for code, name in fg.STATUS_NAMES.items():
+        assert fg.fp8_status_string(code).startswith(name)
+    assert lib.fp8fg_version() >= 100
+
+
+NULL = ctypes.c_void_p(0)
+A16 = ctypes.c_void_p(0x10000)      # 16-byte aligned fake device addresses: never dereferenced,
+A16b = ctypes.c_void_p(0x20000)     # every call below is rejected before any CUDA call
+MIS = ctypes.c_void_p(0x10008)
+
+
+def test_quant_act_rejections(lib):
+    f = lib.fp8_quant_act_1x128
+    assert f(A16, 4, 100, 100, A16b, 100, A16, 1, 4, NULL) == 3            # K % 128
+    assert f(A16, -1, 128, 128, A16b, 128, A16, 1, 4, NULL) == 3           # negative M
+    assert f(A16, 0, 128, 128, A16b, 128, A16, 1, 4, NULL) == 0            # empty: nothing launched
+    assert f(NULL, 4, 128, 128, A16b, 128, A16, 1, 4, NULL) == 1           # null x
+    assert f(A16, 4, 128, 64, A16b, 128, A16, 1, 4, NULL) == 6             # ldx < K
+    assert f(MIS, 4, 128, 128, A16b, 128, A16, 1, 4, NULL) == 2            # misaligned x
+    assert f(A16, 4, 128, 132, A16b, 128, A16, 1, 4, NULL) == 2            # ldx*2 not multiple of 16
+
+
+def test_quant_w_rejections(lib):
+    f = lib.fp8_quant_w_128x128
+    assert f(A16, 256, 200, 200, A16b, 256, 0, A16, 2, 1, NULL) == 3       # N % 128
+    assert f(A16, 256, 256, 256, A16b, 256, 7, A16, 2, 1, NULL) == 6       # bad layout
+    assert f(A16, 256, 256, 256, NULL, 256, 0, A16, 2, 1, NULL) == 1
+    assert f(A16, 256, 256, 256, MIS, 256, 0, A16, 2, 1, NULL) == 2
+
+
+def test_requant_rejections(lib):
+    f = lib.fp8_requant_1x128_to_128x1
+    assert f(A16, 200, 128, 128, A16, 1, 200, A16b, 200, A16, 1, 128, NULL) == 3   # M % 128
+    assert f(A16, 256, 128, 128, NULL, 1, 256, A16b, 256, A16, 1, 128, NULL) == 1
+    assert f(A16, 256, 128, 128, A16, 1, 256, A16b, 128, A16, 1, 128, NULL) == 6   # ldqT < M
+
+
+def test_gemm_rejections(lib):
+    f = lib.fp8_gemm_blockscaled
+    ok = [A16, 256, A16, 1, 256, A16b, 256, A16, 2, 1, 0, A16b, 256, 256, 256, 256, NULL]
+    bad = list(ok); bad[10] = 5
+    assert f(*bad) == 6                                   # sb_kind
+    bad = list(ok); bad[13] = 200
+    assert f(*bad) == 3                                   # M % 128
+    bad = list(ok); bad[15] = 0
+    assert f(*bad) == 3                                   # K == 0 with a non-empty output
+    bad = list(ok); bad[0] = NULL
+    assert f(*bad) == 1
+    bad = list(ok); bad[5] = MIS
+    assert f(*bad) == 2
+    bad = list(ok); bad[1] = 128
+    assert f(*bad) == 6                                   # lda < K
+    bad = list(ok); bad[13] = 0
+    assert f(*bad) == 0                                   # empty output
+
+
+def test_grouped_gemm_rejections(lib):
+    f = lib.fp8_grouped_gemm_blockscaled
+    ok = [A16, 256, A16, 1, 256, A16b, A16, A16, 4, 256, 256, 256, A16b, 256, NULL]
+    bad = list(ok); bad[8] = 0
+    assert f(*bad) == 6                                   # G == 0
+    bad = list(ok); bad[8] = 5000
+    assert f(*bad) == 6                                   # G too large
+    bad = list(ok); bad[7] = NULL
+    assert f(*bad) == 1                                   # offsets
+    bad = list(ok); bad[9] = 100
+    assert f(*bad) == 3                                   # M_total % 128
+    bad = list(ok); bad[7] = ctypes.c_void_p(0x10002)
+    assert f(*bad) == 2
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    x = torch.zeros(4, 128, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        fg.fp8_quant_act_1x128(x)
