@@ -1,0 +1,624 @@
+#!/usr/bin/env python
+"""Benchmark of the fine-grained FP8 hot path on B300.
+
+One step = one pass of the whole path over one batch of synthetic inputs, the
+FP8 training step of a large MoE transformer layer:
+
+  forward of an FP8 linear layer      X bf16 [8192, 7168] -> 1x128 quantize;
+                                      W bf16 [7168, 18432] -> 128x128 quantize;
+                                      Y = GEMM (1x128 x 128x128 scales) bf16 [8192, 18432]
+  weight gradient of that layer       dY bf16 [8192, 18432] -> 1x128 quantize;
+                                      cached Xq and dYq -> 1x128 -> 128x1 requantize;
+                                      dW = GEMM (128x1 x 128x1 scales) bf16 [7168, 18432]
+  MoE expert forward                  16384 tokens x 8 picks (Zipf 1.1 over 32 experts,
+                                      padded to 128 rows) bf16 [~133k, 7168] -> 1x128 quantize;
+                                      32 experts W_g [7168, 2048] -> 128x128 quantize;
+                                      grouped GEMM -> bf16 [~133k, 2048]
+
+`value` is the step's GEMM work (2MNK summed over the three GEMMs, routed rows
+for the MoE) divided by the step time, summed over ranks: whole-step TFLOP/s,
+quantizers included.  Inputs live in HBM before the timed region; every input
+is larger than L2 or is followed by larger traffic.  `e2e` repeats the step
+with the inputs copied from pinned host memory and the outputs read back.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Multi-GPU (torchrun): every rank runs the same step on its own GPU (weak
+scaling, no collective on the data path); the time is the max over ranks.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s (% FP8 peak); quantizer GB/s (% HBM)"
+UNIT = "TFLOP/s"
+FP8_OVER_BF16 = 2.0          # nominal dense FP8 / BF16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+L2_BYTES = 126 * 2 ** 20
+
+# workload sizes
+T, CIN, COUT = 8192, 7168, 18432
+G, MOE_K, MOE_N, TOKENS, TOPK, ZIPF = 32, 7168, 2048, 16384, 8, 1.1
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ workload ----
+
+class Workload:
+    """Host (numpy) inputs of one step plus the algorithmic work of each kernel."""
+
+    def __init__(self, seed_offset=0):
+        s = seed_offset
+        self.x, _ = synth.activation(2 + s, T, CIN)                     # 1% channels x100
+        self.w = synth.weight(2 + s, CIN, COUT)                         # N(0, 0.02^2)
+        self.dy = synth.wgrad_tensor(4 + s, 1, T, COUT)                 # N(0,1e-3^2), 0.1% x1000
+        moe = synth.moe_inputs(seed=5 + s, G=G, K=MOE_K, N=MOE_N, tokens=TOKENS, topk=TOPK, zipf_s=ZIPF)
+        self.moe_x = moe.x
+        self.moe_w = moe.w
+        self.moe_offsets = moe.offsets
+        self.moe_counts = moe.counts
+        self.moe_rows = int(moe.offsets[-1])
+        self.routed_rows = moe.routed_rows
+
+    def gemm_flops(self):
+        return {
+            "gemm_fprop": 2.0 * T * COUT * CIN,
+            "gemm_wgrad": 2.0 * CIN * COUT * T,
+            "grouped_gemm_moe": 2.0 * self.routed_rows * MOE_N * MOE_K,
+        }
+
+    def quant_bytes(self):
+        def q(rows, cols):       # bf16 in, e4m3 out, one fp32 scale per 128 elements
+            return rows * cols * 3 + rows * cols // 128 * 4
+
+        def rq(rows, cols):      # e4m3 + scales in, e4m3 + scales out
+            return 2 * (rows * cols + rows * cols // 128 * 4)
+        return {
+            "quant_act_x": q(T, CIN),
+            "quant_w": q(CIN, COUT) - CIN * COUT // 128 * 4 + (CIN // 128) * (COUT // 128) * 4,
+            "quant_act_dy": q(T, COUT),
+            "requant_x": rq(T, CIN),
+            "requant_dy": rq(T, COUT),
+            "quant_act_moe": q(self.moe_rows, MOE_K),
+            "quant_w_moe": G * (MOE_K * MOE_N * 3 + (MOE_K // 128) * (MOE_N // 128) * 4),
+        }
+
+    def describe(self):
+        return {
+            "workload": "FP8 training step of one MoE transformer layer: linear fwd "
+                        "[8192x7168]x[7168x18432] + wgrad (dW [7168x18432], K=8192 tokens) + "
+                        "MoE grouped fwd (32 experts [7168x2048], 16384 tokens x 8, Zipf 1.1)",
+            "fprop": {"M": T, "N": COUT, "K": CIN},
+            "wgrad": {"M": CIN, "N": COUT, "K": T},
+            "moe": {"experts": G, "N": MOE_N, "K": MOE_K, "routed_rows": self.routed_rows,
+                    "padded_rows": self.moe_rows},
+            "quantizers": "1x128 act [8192x7168], [8192x18432], [%dx7168]; 128x128 weight "
+                          "[7168x18432], 32x[7168x2048]; 1x128->128x1 requant of [8192x7168], "
+                          "[8192x18432]" % self.moe_rows,
+            "l2": "inputs larger than L2 (126 MB); %.1f GB of quantizer traffic per step"
+                  % (sum(self.quant_bytes().values()) / 1e9),
+            "global_batch": T,
+            "parallelism": "replicas",
+        }
+
+
+# -------------------------------------------------------------- device ----
+
+class DeviceStep:
+    """Device buffers and the sequence of library calls of one step."""
+
+    KERNELS = ["quant_act_x", "quant_w", "gemm_fprop", "quant_act_dy", "requant_x", "requant_dy",
+               "gemm_wgrad", "quant_act_moe", "quant_w_moe", "grouped_gemm_moe"]
+    LAUNCHES_PER_STEP = 9 + G   # 32 per-expert weight quantizations
+
+    def __init__(self, wl, device):
+        import torch
+        import fp8_fine_grained_20_b300 as fg
+        self.fg = fg
+        self.torch = torch
+        self.dev = device
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+
+        def e(shape, dt):
+            return torch.empty(shape, dtype=dt, device=device)
+
+        # inputs
+        self.x = e((T, CIN), bf)
+        self.w = e((CIN, COUT), bf)
+        self.dy = e((T, COUT), bf)
+        self.moe_x = e((wl.moe_rows, MOE_K), bf)
+        self.moe_w = e((G, MOE_K, MOE_N), bf)
+        self.moe_off = e((G + 1,), torch.int32)
+        # intermediates (scales MN-major: logical [rows, groups] views with stride 1 along rows)
+        self.xq, self.sx = e((T, CIN), u8), e((CIN // 128, T), f32).t()
+        self.wq, self.sw = e((COUT, CIN), u8), e((CIN // 128, COUT // 128), f32)
+        self.dyq, self.sdy = e((T, COUT), u8), e((COUT // 128, T), f32).t()
+        self.xqT, self.sxT = e((CIN, T), u8), e((T // 128, CIN), f32).t()
+        self.dyqT, self.sdyT = e((COUT, T), u8), e((T // 128, COUT), f32).t()
+        self.mxq, self.smx = e((wl.moe_rows, MOE_K), u8), e((MOE_K // 128, wl.moe_rows), f32).t()
+        self.mwq, self.smw = e((G, MOE_N, MOE_K), u8), e((G, MOE_K // 128, MOE_N // 128), f32)
+        # outputs
+        self.y = e((T, COUT), bf)
+        self.dw = e((CIN, COUT), bf)
+        self.moe_y = e((wl.moe_rows, MOE_N), bf)
+        self.load_inputs(wl)
+
+    def load_inputs(self, wl):
+        torch = self.torch
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+        self.x.copy_(bf16(wl.x))
+        self.w.copy_(bf16(wl.w))
+        self.dy.copy_(bf16(wl.dy))
+        self.moe_x.copy_(bf16(wl.moe_x))
+        self.moe_w.copy_(bf16(wl.moe_w))
+        self.moe_off.copy_(torch.from_numpy(wl.moe_offsets))
+        torch.cuda.synchronize()
+
+    def run(self, stream, ev=None):
+        """Launch one step on `stream`.  `ev`, if given, maps kernel name ->
+        (start_event, end_event) recorded around that kernel's launches."""
+        fg = self.fg
+
+        def rec(name, i):
+            if ev is not None:
+                ev[name][i].record(stream)
+
+        rec("quant_act_x", 0)
+        fg.fp8_quant_act_1x128(self.x, self.xq, self.sx, stream=stream)
+        rec("quant_act_x", 1)
+        rec("quant_w", 0)
+        fg.fp8_quant_w_128x128(self.w, self.wq, self.sw, stream=stream)
+        rec("quant_w", 1)
+        rec("gemm_fprop", 0)
+        fg.fp8_gemm_blockscaled(self.xq, self.sx, self.wq, self.sw, fg.FP8_SB_BLOCK128x128, self.y,
+                                stream=stream)
+        rec("gemm_fprop", 1)
+        rec("quant_act_dy", 0)
+        fg.fp8_quant_act_1x128(self.dy, self.dyq, self.sdy, stream=stream)
+        rec("quant_act_dy", 1)
+        rec("requant_x", 0)
+        fg.fp8_requant_1x128_to_128x1(self.xq, self.sx, self.xqT, self.sxT, stream=stream)
+        rec("requant_x", 1)
+        rec("requant_dy", 0)
+        fg.fp8_requant_1x128_to_128x1(self.dyq, self.sdy, self.dyqT, self.sdyT, stream=stream)
+        rec("requant_dy", 1)
+        rec("gemm_wgrad", 0)
+        fg.fp8_gemm_blockscaled(self.xqT, self.sxT, self.dyqT, self.sdyT.t(), fg.FP8_SB_COL128x1, self.dw,
+                                stream=stream)
+        rec("gemm_wgrad", 1)
+        rec("quant_act_moe", 0)
+        fg.fp8_quant_act_1x128(self.moe_x, self.mxq, self.smx, stream=stream)
+        rec("quant_act_moe", 1)
+        rec("quant_w_moe", 0)
+        for g in range(G):
+            fg.fp8_quant_w_128x128(self.moe_w[g], self.mwq[g], self.smw[g], stream=stream)
+        rec("quant_w_moe", 1)
+        rec("grouped_gemm_moe", 0)
+        fg.fp8_grouped_gemm_blockscaled(self.mxq, self.smx, self.mwq, self.smw, self.moe_off, self.moe_y,
+                                        stream=stream)
+        rec("grouped_gemm_moe", 1)
+
+
+# ------------------------------------------------------------- helpers ----
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {k: float(pk[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("ptx.cuh", "quant.cuh", "gemm.cuh", "fp8fg.cu"):
+        with open(os.path.join(ROOT, "fp8_fine_grained_20_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """Per-launch DRAM bytes of each kernel from the committed ncu summary, valid
+    only while the kernel sources are unchanged since the capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if t.get("source_hash") != kernel_source_hash():
+        return {}
+    return t.get("bytes_per_launch", {})
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "fp8fg_clocks_%d_%s.csv" % (os.getpid(), str(gpu_index).replace(":", "_")))
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_median": statistics.median(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------- CPU oracle leg ----
+
+def smi_id(torch, local):
+    """nvidia-smi selector of this rank's GPU: its PCI bus id when torch knows it."""
+    p = torch.cuda.get_device_properties(local)
+    try:
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except AttributeError:
+        return str(local)
+
+
+def cpu_oracle_sample(wl, frac, threads=1):
+    """Run the CPU oracle on a bounded sample of the step: a fraction `frac` of
+    every quantizer's groups and of every GEMM's output elements.  Returns
+    (seconds, description, extrapolated full-step seconds)."""
+    import oracle
+    rng = np.random.default_rng(0)
+    t_total = 0.0
+    parts = []
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        out = fn()
+        return out, time.perf_counter() - t0
+
+    # 1x128 activation quantization: whole rows
+    act_elems = {"x": (wl.x, T * CIN), "dy": (wl.dy, T * COUT), "moe": (wl.moe_x, wl.moe_rows * MOE_K)}
+    est = 0.0
+    for name, (arr, n_full) in act_elems.items():
+        rows = max(1, int(round(frac * arr.shape[0])))
+        (q, s), dt = timed(lambda: oracle.quant_act_1x128(arr[:rows], threads=threads))
+        t_total += dt
+        est += dt * n_full / (rows * arr.shape[1])
+        parts.append("act %s %d rows" % (name, rows))
+    # 128x128 weight quantization: one 128-row block strip, a fraction of its columns
+    for name, arr, n_full in (("w", wl.w, CIN * COUT), ("moe_w", wl.moe_w[0], G * MOE_K * MOE_N)):
+        cols = max(128, int(round(frac * arr.size / 128)) // 128 * 128)
+        cols = min(cols, arr.shape[1])
+        _, dt = timed(lambda: oracle.quant_w_128x128(np.ascontiguousarray(arr[:128, :cols]), threads=threads))
+        t_total += dt
+        est += dt * n_full / (128 * cols)
+        parts.append("weight %s 128x%d" % (name, cols))
+    # requantization: one 128-token block x a fraction of the channels
+    for name, arr, n_full in (("x", wl.x, T * CIN), ("dy", wl.dy, T * COUT)):
+        q, s = oracle.quant_act_1x128(arr[:128])
+        cols = min(arr.shape[1], max(128, int(round(frac * arr.size / 128)) // 128 * 128))
+        _, dt = timed(lambda: oracle.requant_1x128_to_128x1(np.ascontiguousarray(q[:, :cols]),
+                                                            np.ascontiguousarray(s[:, :cols // 128]),
+                                                            threads=threads))
+        t_total += dt
+        est += dt * n_full / (128 * cols)
+        parts.append("requant %s 128x%d" % (name, cols))
+    # GEMMs: sampled output elements (operands: oracle-quantized strips)
+    xq, xs = oracle.quant_act_1x128(wl.x[:128])
+    wq, ws = oracle.quant_w_128x128(np.ascontiguousarray(wl.w[:, :128]))
+    wt = np.ascontiguousarray(wq.T)
+    for name, n_out in (("fprop", T * COUT), ("wgrad", CIN * COUT), ("moe", wl.routed_rows * MOE_N)):
+        k = T if name == "wgrad" else CIN
+        cnt = max(16, int(round(frac * n_out)))
+        ms = rng.integers(0, 128, cnt)
+        ns = rng.integers(0, 128, cnt)
+        if k == CIN:
+            a, sa, b, sb = xq, xs, wt, ws
+        else:  # K = 8192 tokens: tile the 7168-deep strips up to the token count
+            reps = -(-T // CIN)
+            a = np.tile(xq, (1, reps))[:, :T]
+            sa = np.tile(xs, (1, reps))[:, :T // 128]
+            b = np.tile(wt, (1, reps))[:, :T]
+            sb = np.tile(ws, (reps, 1))[:T // 128]
+        _, dt = timed(lambda: oracle.gemm_blockscaled_sample(a, sa, b, sb, oracle.SB_BLOCK128x128, ms, ns,
+                                                             threads=threads))
+        t_total += dt
+        est += dt * n_out / cnt
+        parts.append("%s %d outputs" % (name, cnt))
+    return t_total, "; ".join(parts), est
+
+
+def calibrate_frac(wl, target_seconds):
+    """Fraction of the step whose oracle run takes about `target_seconds`."""
+    probe = 2e-5
+    t, _, est = cpu_oracle_sample(wl, probe)
+    return min(1.0, max(1e-7, target_seconds / max(est, 1e-9))), est
+
+
+# --------------------------------------------------------------- main ----
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: rank 0 only, bounded samples."""
+    if rank != 0:
+        return
+    wl = Workload()
+    flops = sum(wl.gemm_flops().values())
+    per_step = max(0.05, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    frac, est_full = calibrate_frac(wl, per_step)
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, frac)
+    samples, ests = [], []
+    desc = ""
+    for _ in range(args.steps):
+        t, desc, est = cpu_oracle_sample(wl, frac)
+        samples.append(t)
+        ests.append(est)
+    est_step = statistics.mean(ests)
+    value = flops / est_step / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": est_step * 1e3,
+        "sample_ms_per_step": statistics.mean(samples) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": wl.describe(),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "fraction %.3g of each kernel's work per step: %s" % (frac, desc)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import torch
+    import torch.distributed as dist
+    import fp8_fine_grained_20_b300 as fg
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    fg.capi()
+
+    wl = Workload(seed_offset=0)
+    step = DeviceStep(wl, device)
+    stream = torch.cuda.Stream(device=device)
+    flops = wl.gemm_flops()
+    qbytes = wl.quant_bytes()
+    total_flops = sum(flops.values())
+
+    # warm-up
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step.run(stream)
+    torch.cuda.synchronize()
+    if fg.fp8_get_device_status(reset=True) != 0:
+        raise SystemExit("device status set during warm-up")
+
+    # timed region: K steps, per-kernel events inside, clocks sampled alongside
+    evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for k in DeviceStep.KERNELS} for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(smi_id(torch, local))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            step.run(stream, evs[i])
+        t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    status = fg.fp8_get_device_status(reset=True)
+    ms_step = ms_total / args.steps
+    value = world * total_flops / (ms_step * 1e-3) / 1e12
+
+    per_kernel_ms = {k: statistics.mean(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(args.steps))
+                     for k in DeviceStep.KERNELS}
+    peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    fp8_peak_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
+    hbm = peaks["hbm_gbs"]
+    traffic = load_traffic()
+    kernels = {}
+    for k, ms in per_kernel_ms.items():
+        launches = G if k == "quant_w_moe" else 1
+        d = {"ms": ms, "launches_per_step": launches}
+        if k in flops:
+            tf = flops[k] / (ms * 1e-3) / 1e12
+            d.update({"tflops": tf, "frac_fp8_sustained": tf / fp8_peak, "frac_fp8_burst": tf / fp8_peak_burst})
+        else:
+            gbs = qbytes[k] / (ms * 1e-3) / 1e9
+            d.update({"gbs": gbs, "frac_hbm": gbs / hbm, "bytes": qbytes[k]})
+        kernels[k] = d
+    dom = max(per_kernel_ms, key=per_kernel_ms.get)
+    if dom in flops:
+        ach = flops[dom] / (per_kernel_ms[dom] * 1e-3) / 1e12
+        roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
+                    "frac": ach / fp8_peak, "traffic": traffic.get(dom),
+                    "peak_source": "%s sustained bf16 x %.0f (nominal FP8/BF16 ratio)" % (peak_src, FP8_OVER_BF16)}
+    else:
+        launches = kernels[dom]["launches_per_step"]
+        ach = qbytes[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
+        roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+                    "frac": ach / hbm, "traffic": traffic.get(dom), "peak_source": peak_src + " copy"}
+    if roofline["traffic"] is not None:
+        roofline["traffic"] = float(roofline["traffic"])
+
+    # end-to-end: pinned host inputs -> device -> step -> outputs back to pinned host
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, step, stream, total_flops, world, device)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        frac, _ = calibrate_frac(wl, args.cpu_seconds)
+        secs, desc, est = cpu_oracle_sample(wl, frac)
+        cpu = {"value": total_flops / est / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "fraction %.3g of every kernel's work (%s), %.1f s measured, extrapolated to the "
+                         "whole step" % (frac, desc, secs)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic", "config": wl.describe(),
+            "roofline": roofline, "kernels": kernels,
+            "quantizers_gbs": sum(qbytes.values()) / (sum(per_kernel_ms[k] for k in qbytes) * 1e-3) / 1e9,
+            "gemms_tflops": total_flops / (sum(per_kernel_ms[k] for k in flops) * 1e-3) / 1e12,
+            "fp8_peak_tflops": {"sustained": fp8_peak, "burst": fp8_peak_burst, "source": peak_src},
+            "hbm_peak_gbs": hbm,
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": DeviceStep.LAUNCHES_PER_STEP * args.steps,
+            "clocks": clk, "device_status": status,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, step, stream, total_flops, world, device):
+    import torch
+    import torch.distributed as dist
+
+    def pinned(a, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            t = t.view(dtype)
+        return t.pin_memory()
+    h_in = [(pinned(wl.x.view(np.int16), torch.bfloat16), step.x),
+            (pinned(wl.w.view(np.int16), torch.bfloat16), step.w),
+            (pinned(wl.dy.view(np.int16), torch.bfloat16), step.dy),
+            (pinned(wl.moe_x.view(np.int16), torch.bfloat16), step.moe_x),
+            (pinned(wl.moe_w.view(np.int16), torch.bfloat16), step.moe_w),
+            (pinned(wl.moe_offsets), step.moe_off)]
+    h_out = [(step.y, torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()),
+             (step.dw, torch.empty(step.dw.shape, dtype=step.dw.dtype).pin_memory()),
+             (step.moe_y, torch.empty(step.moe_y.shape, dtype=step.moe_y.dtype).pin_memory())]
+    h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
+    d2h = sum(h.numel() * h.element_size() for _, h in h_out)
+
+    def one():
+        for h, d in h_in:
+            d.copy_(h, non_blocking=True)
+        step.run(stream)
+        for d, h in h_out:
+            h.copy_(d, non_blocking=True)
+    with torch.cuda.stream(stream):
+        one()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            one()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    ms_step = ms / args.e2e_steps
+    # restore the device-resident inputs used by later legs
+    step.load_inputs(wl)
+    return {"value": world * total_flops / (ms_step * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_step,
+            "steps": args.e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    main()
