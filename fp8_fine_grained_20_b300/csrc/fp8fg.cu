@@ -161,11 +161,11 @@ fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_
     const int dev = current_device();
     const int sms = sm_count(dev);
     if (sms <= 0) return FP8_ERR_CUDA;
-    constexpr int UNROLL = 4;
+    constexpr int UNROLL = 2;
     auto kernel = k_quant_act_1x128<UNROLL>;
     const int per_sm = blocks_per_sm(kernel, 256, dev, occ);
-    const int64_t pairs = (M * KB + 1) / 2;
-    const int64_t want = ceil_div(pairs, 8 * UNROLL);  // 8 warps per CTA, UNROLL pairs each
+    const int64_t slots = ceil_div(M * KB, 8);           // a warp quantizes 8 groups per slot
+    const int64_t want = ceil_div(slots, 8 * UNROLL);    // 8 warps per CTA, UNROLL slots each
     const int64_t cap = static_cast<int64_t>(sms) * per_sm;
     const int grid = static_cast<int>(want < cap ? want : cap);
     kernel<<<grid, 256, 0, as_stream(stream)>>>(x, static_cast<int>(M), static_cast<int>(KB), ldx, q, ldq, s,

@@ -7,15 +7,24 @@
 // with both divisions IEEE fp32 round-to-nearest-even (scaling rule of
 // why-be.why-be.co.kr post 65900: largest magnitude onto the FP8 maximum).
 //
-// Exact division without paying for it on every element: with r = RN(1/s),
-// q0 = RN(|x| * r) lies within 5 fp32 ulps of RN(|x| / s) (relative error of
-// r and of the product, each <= 2^-24, plus the final rounding; one binade
-// boundary at most doubles the count).  E4M3 rounding is monotonic in the
-// fp32 bit pattern of a non-negative value, so if the codes of the bit
-// patterns q0 - 8 and q0 + 8 agree, that is the code of RN(|x| / s); only when
-// an E4M3 rounding boundary lies inside that window (about 16 in 2^20 values)
-// is the exact IEEE quotient computed.  Groups whose scale is an fp32
-// subnormal (1/s would overflow) always take the exact quotient.
+// The quotient x / s must be the correctly rounded fp32 value, because E4M3
+// rounds it a second time: with bf16 inputs the exact ratio lands on an E4M3
+// rounding boundary for about 0.5% of the elements (exact ties, and values one
+// fp32 ulp from a tie because s itself is rounded), so an approximate quotient
+// is not enough.  Per group the kernels compute s = RN(amax / 448) and
+// r = RN(1 / s) with IEEE division and reciprocal; per element they use
+// Markstein's correction (P. Markstein, "Computation of elementary functions
+// on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): if r
+// is within half an ulp of 1/s and q is within one ulp of x/s, the remainder
+// e = x - q s is exact in one FMA and RN(q + e r) is RN(x/s).  q0 = RN(x r) can
+// be up to 1.5 ulps away, so two correction steps are applied (the first one
+// makes the value faithful, the second one exact):
+//     q0 = x r;  q1 = q0 + (x - q0 s) r;  q = q1 + (x - q1 s) r
+// as packed FP32x2 multiplies/FMAs on pairs of elements, followed by one
+// E4M3x2 conversion (round to nearest even, saturating).  The sign bit of
+// each input is OR-ed into its code, so -0 and negative values that round to
+// zero keep the sign.  Groups with amax == 0 give zero codes; groups whose
+// scale is below 2^-92 use IEEE division per element.
 #pragma once
 
 #include "ptx.cuh"
@@ -23,62 +32,93 @@
 namespace fp8fg {
 
 constexpr float kE4M3Max = 448.0f;
-constexpr float kFltMinNormal = 1.17549435082228750797e-38f;
+// Smallest scale for the reciprocal path: every element whose E4M3 code can
+// be nonzero (x / s >= 2^-11) is then >= 2^-103, so the correction remainders
+// (granularity about x 2^-46) stay in the normal fp32 range and are exact.
+constexpr float kMinRecipScale = 0x1p-92f;
 
 struct GroupScale {
-    float s;    // amax / 448
+    float s;    // amax / 448 (IEEE division)
     float r;    // RN(1 / s)
-    int mode;   // 0: all-zero group, 1: fast path valid, 2: exact quotient only
+    int mode;   // 0: all-zero group, 1: reciprocal path, 2: IEEE division per element (tiny s)
 };
 
 __device__ __forceinline__ GroupScale group_scale(float amax) {
     GroupScale g;
     g.s = __fdiv_rn(amax, kE4M3Max);
     g.r = __frcp_rn(g.s);
-    g.mode = (amax == 0.0f) ? 0 : (g.s >= kFltMinNormal ? 1 : 2);
+    g.mode = (amax == 0.0f) ? 0 : (g.s >= kMinRecipScale ? 1 : 2);
     return g;
 }
 
-// E4M3 code (sign included) of the fp32 quotient x / s.
-__device__ __forceinline__ uint32_t quant_code(float x, const GroupScale& g) {
-    const uint32_t sign = (__float_as_uint(x) >> 24) & 0x80u;
-    const float ax = fabsf(x);
-    uint32_t c;
-    if (g.mode == 1) {
-        const uint32_t b = __float_as_uint(__fmul_rn(ax, g.r));
-        const uint32_t lo = max(b, 8u) - 8u;
-        const uint32_t c2 = cvt_e4m3x2(__uint_as_float(b + 8u), __uint_as_float(lo));
-        c = c2 & 0xFFu;
-        if (c != (c2 >> 8)) c = cvt_e4m3x2(0.0f, __fdiv_rn(ax, g.s)) & 0xFFu;
-    } else if (g.mode == 2) {
-        c = cvt_e4m3x2(0.0f, __fdiv_rn(ax, g.s)) & 0xFFu;
-    } else {
-        return 0u;
-    }
-    return c | sign;
+// RN(x / s) for a pair of values by Markstein's two-step correction; r2 =
+// (RN(1/s0), RN(1/s1)), ns2 = (-s0, -s1).
+__device__ __forceinline__ float2 div2_markstein(float2 x, float2 r2, float2 ns2) {
+    const float2 q0 = __fmul2_rn(x, r2);
+    const float2 e0 = __ffma2_rn(q0, ns2, x);
+    const float2 q1 = __ffma2_rn(e0, r2, q0);
+    const float2 e1 = __ffma2_rn(q1, ns2, x);
+    return __ffma2_rn(e1, r2, q1);
 }
 
-// Four codes packed little-endian into one word.
-__device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, const GroupScale& g) {
-    return quant_code(a, g) | (quant_code(b, g) << 8) | (quant_code(c, g) << 16) | (quant_code(d, g) << 24);
+// Magnitude-only E4M3 codes of a pair (bits 7:0 from x.x, 15:8 from x.y); the
+// sign bits are applied by the caller.
+__device__ __forceinline__ uint32_t e4m3_pair(float2 q) { return cvt_e4m3x2(q.y, q.x); }
+
+// Elementwise max of two pairs of 16-bit unsigned values.
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ float absmax8(const uint4& v) {
-    float a = fmaxf(fabsf(bf16lo(v.x)), fabsf(bf16hi(v.x)));
-    a = fmaxf(a, fmaxf(fabsf(bf16lo(v.y)), fabsf(bf16hi(v.y))));
-    a = fmaxf(a, fmaxf(fabsf(bf16lo(v.z)), fabsf(bf16hi(v.z))));
-    a = fmaxf(a, fmaxf(fabsf(bf16lo(v.w)), fabsf(bf16hi(v.w))));
-    return a;
+// Magnitude max of eight bf16 values as an |bf16|x2 word: with the sign bits
+// cleared, the integer order of finite bf16 patterns is the order of values.
+__device__ __forceinline__ uint32_t absmax_bf16x8(const uint4& v) {
+    const uint32_t m = 0x7FFF7FFFu;
+    return umax16x2(umax16x2(v.x & m, v.y & m), umax16x2(v.z & m, v.w & m));
 }
 
+// fp32 value of the larger half of an |bf16|x2 word.
+__device__ __forceinline__ float hmax_bf16x2_to_f32(uint32_t w) {
+    const uint32_t hi = w >> 16, lo = w & 0xFFFFu;
+    return __uint_as_float((hi > lo ? hi : lo) << 16);
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f32x2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// E4M3 code (sign included) of RN(x / s) by IEEE division; mode as in GroupScale.
+__device__ __forceinline__ uint32_t quant_div(float x, float s, int mode) {
+    if (mode == 0) return 0u;
+    const uint32_t c = cvt_e4m3x2(0.0f, __fdiv_rn(fabsf(x), s)) & 0xFFu;
+    return c | ((__float_as_uint(x) >> 24) & 0x80u);
+}
+
+// Eight codes of eight bf16 values (one 16-byte chunk) of one group.
 __device__ __forceinline__ uint2 quant8_bf16(const uint4& v, const GroupScale& g) {
-    uint2 o;
-    o.x = quant4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y), g);
-    o.y = quant4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w), g);
-    return o;
+    if (g.mode == 1) {
+        const float2 r2 = make_float2(g.r, g.r);
+        const float2 ns2 = make_float2(-g.s, -g.s);
+        const uint32_t c0 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.x), r2, ns2));
+        const uint32_t c1 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.y), r2, ns2));
+        const uint32_t c2 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.z), r2, ns2));
+        const uint32_t c3 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.w), r2, ns2));
+        // sign bits (bit 15 of each bf16) into bit 7 of each code byte
+        const uint32_t sx = __byte_perm(v.x, v.y, 0x7531) & 0x80808080u;
+        const uint32_t sy = __byte_perm(v.z, v.w, 0x7531) & 0x80808080u;
+        return make_uint2(__byte_perm(c0, c1, 0x5410) | sx, __byte_perm(c2, c3, 0x5410) | sy);
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 f = bf16x2_to_f32x2(w[k]);
+        const uint32_t c = quant_div(f.x, g.s, g.mode) | (quant_div(f.y, g.s, g.mode) << 8);
+        o[k >> 1] |= c << (16 * (k & 1));
+    }
+    return make_uint2(o[0], o[1]);
 }
 
 // Transpose an 8x8 byte matrix held as rows (r[i].x = bytes 0-3, r[i].y =
@@ -107,38 +147,41 @@ __device__ __forceinline__ void transpose8x8(const uint2 (&r)[8], uint2 (&c)[8])
 
 // ------------------------------------------------- 1x128 activations ----
 //
-// A half-warp owns one group: 16 lanes x 16 bytes = 128 bf16.  Each warp
-// processes UNROLL group pairs per iteration, all loads issued before any
-// reduction, over a grid-stride loop in row-major group order.
+// Four lanes own one group (128 bf16 = 16 chunks of 16 bytes; lane l%4 loads
+// chunks l%4, l%4+4, l%4+8, l%4+12), so a warp covers 8 consecutive groups
+// per slot and each lane quantizes 32 values with one scale computation.
+// UNROLL slots per iteration keep 4*UNROLL 16-byte loads in flight per lane;
+// grid-stride over slots in row-major group order.
 template <int UNROLL>
 __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restrict__ x, int M, int KB,
                                                          int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
                                                          float* __restrict__ s, int64_t ssm, int64_t sskb) {
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4;
-    const int hl = lane & 15;
+    const int sub = lane & 3;                  // chunk phase inside the group
     const int64_t n_groups = static_cast<int64_t>(M) * KB;
-    const int64_t n_pairs = (n_groups + 1) >> 1;
+    const int64_t n_slots = (n_groups + 7) >> 3;
     const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
     const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
 
-    // (m, kb) of this lane's current group and the per-step advance by 2*nw groups
-    const int64_t step = 2 * nw;
+    // (m, kb) of this lane's group in the current slot; advance by 8*nw groups per slot
+    const int64_t step = 8 * nw;
     const int step_m = static_cast<int>(step / KB);
     const int step_kb = static_cast<int>(step % KB);
-    const int64_t g0 = 2 * wid + half;
+    const int64_t g0 = 8 * wid + (lane >> 2);
     int m = static_cast<int>(g0 / KB);
     int kb = static_cast<int>(g0 % KB);
 
-    for (int64_t p0 = wid; p0 < n_pairs; p0 += nw * UNROLL) {
-        uint4 v[UNROLL];
+    for (int64_t p0 = wid; p0 < n_slots; p0 += nw * UNROLL) {
+        uint4 v[UNROLL][4];
         int mu[UNROLL], kbu[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             mu[u] = m;
             kbu[u] = kb;
-            v[u] = (m < M) ? ldg_nc_v4(x + static_cast<int64_t>(m) * ldx + kb * 128 + hl * 8)
-                           : make_uint4(0u, 0u, 0u, 0u);
+            const uint16_t* src = x + static_cast<int64_t>(m) * ldx + kb * 128 + sub * 8;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[u][i] = (m < M) ? ldg_nc_v4(src + 32 * i) : make_uint4(0u, 0u, 0u, 0u);
             m += step_m;
             kb += step_kb;
             if (kb >= KB) {
@@ -148,15 +191,17 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            float a = absmax8(v[u]);
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
+            const uint32_t h = umax16x2(umax16x2(absmax_bf16x8(v[u][0]), absmax_bf16x8(v[u][1])),
+                                        umax16x2(absmax_bf16x8(v[u][2]), absmax_bf16x8(v[u][3])));
+            float a = hmax_bf16x2_to_f32(h);
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
             if (mu[u] < M) {
                 const GroupScale g = group_scale(a);
-                stg_v2(q + static_cast<int64_t>(mu[u]) * ldq + kbu[u] * 128 + hl * 8, quant8_bf16(v[u], g));
-                if (hl == 0) s[static_cast<int64_t>(mu[u]) * ssm + static_cast<int64_t>(kbu[u]) * sskb] = g.s;
+                uint8_t* dst = q + static_cast<int64_t>(mu[u]) * ldq + kbu[u] * 128 + sub * 8;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) stg_v2(dst + 32 * i, quant8_bf16(v[u][i], g));
+                if (sub == 0) s[static_cast<int64_t>(mu[u]) * ssm + static_cast<int64_t>(kbu[u]) * sskb] = g.s;
             }
         }
     }
@@ -167,29 +212,42 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
 // One CTA (256 threads) per 128x128 block per iteration.  Thread (warp w,
 // lane l) holds rows 8*rb .. 8*rb+7 (rb = 2w + l/16) and columns 8*(l%16) ..
 // +7 of the block: eight 16-byte loads, each row segment read by 16
-// consecutive lanes.  The block amax is reduced through shared memory; the
+// consecutive lanes; the next block's loads are issued before the current
+// block is processed.  The block amax is reduced through shared memory; the
 // K-major output layout is produced by an in-register 8x8 byte transpose.
-__global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restrict__ w, int KB, int NB,
-                                                         int64_t ldw, uint8_t* __restrict__ q, int64_t ldq,
-                                                         int kmajor, float* __restrict__ s, int64_t sskb,
-                                                         int64_t ssnb) {
+__global__ void __launch_bounds__(256, 2) k_quant_w_128x128(const uint16_t* __restrict__ w, int KB, int NB,
+                                                            int64_t ldw, uint8_t* __restrict__ q, int64_t ldq,
+                                                            int kmajor, float* __restrict__ s, int64_t sskb,
+                                                            int64_t ssnb) {
     __shared__ float red[2][8];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nc = lane & 15;
     const int rb = warp * 2 + (lane >> 4);
+    const int n_blocks = KB * NB;
+    int blk = blockIdx.x;
+    if (blk >= n_blocks) return;
+    uint4 v[8];
+    auto load = [&](int b, uint4 (&dst)[8]) {
+        const int kb_ = b / NB;
+        const int nb_ = b - kb_ * NB;
+        const uint16_t* src = w + (static_cast<int64_t>(kb_) * 128 + rb * 8) * ldw + nb_ * 128 + nc * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = ldg_nc_v4(src + i * ldw);
+    };
+    load(blk, v);
     int par = 0;
-    for (int blk = blockIdx.x; blk < KB * NB; blk += gridDim.x, par ^= 1) {
+    for (; blk < n_blocks; blk += gridDim.x, par ^= 1) {
         const int kb = blk / NB;
         const int nb = blk - kb * NB;
         const int64_t row0 = static_cast<int64_t>(kb) * 128 + rb * 8;
-        const uint16_t* src = w + row0 * ldw + nb * 128 + nc * 8;
-        uint4 v[8];
+        uint4 vn[8];
+        const int nxt = blk + gridDim.x;
+        if (nxt < n_blocks) load(nxt, vn);
+        uint32_t h = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = ldg_nc_v4(src + i * ldw);
-        float a = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaxf(a, absmax8(v[i]));
+        for (int i = 0; i < 8; ++i) h = umax16x2(h, absmax_bf16x8(v[i]));
+        float a = hmax_bf16x2_to_f32(h);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
         if (lane == 0) red[par][warp] = a;
@@ -212,93 +270,156 @@ __global__ void __launch_bounds__(256) k_quant_w_128x128(const uint16_t* __restr
             for (int j = 0; j < 8; ++j) stg_v2(q + (n0 + j) * ldq + row0, cols[j]);
         }
         if (threadIdx.x == 0) s[static_cast<int64_t>(kb) * sskb + static_cast<int64_t>(nb) * ssnb] = g.s;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = vn[i];
     }
 }
 
 // ------------------------------------------- 1x128 -> 128x1 requantizer ----
-//
+
+// Eight E4M3 codes (bytes of v, in order) -> eight fp32 values decode(q) * scale,
+// one fp32 multiply each (E4M3 -> f16 -> f32 is exact).
+__device__ __forceinline__ void dequant8(const uint2 v, float scale, float2 (&xr)[4]) {
+    const uint32_t h[4] = {cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.x & 0xFFFFu)),
+                           cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.x >> 16)),
+                           cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.y & 0xFFFFu)),
+                           cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.y >> 16))};
+    const float2 sc = make_float2(scale, scale);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        xr[k] = __fmul2_rn(make_float2(f16_bits_to_f32(h[k] & 0xFFFFu), f16_bits_to_f32(h[k] >> 16)), sc);
+}
+
 // One CTA per 128 (rows) x 128 (channels) block per iteration.  Thread layout
-// as in the weight quantizer, on bytes: eight 8-byte loads of codes, the eight
-// row scales of its rows; dequantization in fp32 (exact E4M3 -> f16 -> f32
-// conversion, then one fp32 multiply); per-channel amax over the 128 rows via
-// a lane shuffle and shared memory; quantization; 8x8 byte transpose; 8-byte
-// stores into the transposed output.
-__global__ void __launch_bounds__(256) k_requant_1x128_to_128x1(const uint8_t* __restrict__ q, int MB, int KB,
-                                                                int64_t ldq, const float* __restrict__ s,
-                                                                int64_t ssm, int64_t sskb,
-                                                                uint8_t* __restrict__ qT, int64_t ldqT,
-                                                                float* __restrict__ sT, int64_t sTk,
-                                                                int64_t sTmb) {
+// as in the weight quantizer, on bytes: eight 8-byte loads of codes and the
+// eight row scales of its rows (the next block's are loaded before the
+// current block is processed).  Pass 1 dequantizes (one fp32 multiply) and
+// reduces the per-channel amax over the 128 rows (lane shuffle + shared
+// memory); one thread per channel derives the channel's scale and reciprocal;
+// pass 2 dequantizes again and quantizes; an 8x8 byte transpose and 8-byte
+// stores write the transposed output.  The sign of every dequantized value is
+// the sign bit of its input code, so the input bytes supply the sign bits.
+__global__ void __launch_bounds__(256, 2) k_requant_1x128_to_128x1(const uint8_t* __restrict__ q, int MB, int KB,
+                                                                   int64_t ldq, const float* __restrict__ s,
+                                                                   int64_t ssm, int64_t sskb,
+                                                                   uint8_t* __restrict__ qT, int64_t ldqT,
+                                                                   float* __restrict__ sT, int64_t sTk,
+                                                                   int64_t sTmb) {
     __shared__ __align__(16) float red[2][8][128];
+    __shared__ __align__(16) float c_s[2][128];
+    __shared__ __align__(16) float c_r[2][128];
+    __shared__ __align__(16) int c_mode[2][128];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nc = lane & 15;
     const int rb = warp * 2 + (lane >> 4);
+    const int n_blocks = MB * KB;
+    int blk = blockIdx.x;
+    if (blk >= n_blocks) return;
+    uint2 v[8];
+    float sr[8];
+    auto load = [&](int b, uint2 (&dv)[8], float (&ds)[8]) {
+        const int mb_ = b / KB;
+        const int kb_ = b - mb_ * KB;
+        const int64_t r0 = static_cast<int64_t>(mb_) * 128 + rb * 8;
+        const int64_t c0 = static_cast<int64_t>(kb_) * 128 + nc * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dv[i] = ldg_nc_v2(q + (r0 + i) * ldq + c0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ds[i] = __ldg(s + (r0 + i) * ssm + static_cast<int64_t>(kb_) * sskb);
+    };
+    load(blk, v, sr);
     int par = 0;
-    for (int blk = blockIdx.x; blk < MB * KB; blk += gridDim.x, par ^= 1) {
+    for (; blk < n_blocks; blk += gridDim.x, par ^= 1) {
         const int mb = blk / KB;
         const int kb = blk - mb * KB;
         const int64_t row0 = static_cast<int64_t>(mb) * 128 + rb * 8;
         const int64_t col0 = static_cast<int64_t>(kb) * 128 + nc * 8;
-        uint2 v[8];
-        float sr[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = ldg_nc_v2(q + (row0 + i) * ldq + col0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) sr[i] = __ldg(s + (row0 + i) * ssm + static_cast<int64_t>(kb) * sskb);
-        float xh[8][8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t h01 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].x & 0xFFFFu));
-            const uint32_t h23 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].x >> 16));
-            const uint32_t h45 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].y & 0xFFFFu));
-            const uint32_t h67 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v[i].y >> 16));
-            xh[i][0] = __fmul_rn(f16_bits_to_f32(h01 & 0xFFFFu), sr[i]);
-            xh[i][1] = __fmul_rn(f16_bits_to_f32(h01 >> 16), sr[i]);
-            xh[i][2] = __fmul_rn(f16_bits_to_f32(h23 & 0xFFFFu), sr[i]);
-            xh[i][3] = __fmul_rn(f16_bits_to_f32(h23 >> 16), sr[i]);
-            xh[i][4] = __fmul_rn(f16_bits_to_f32(h45 & 0xFFFFu), sr[i]);
-            xh[i][5] = __fmul_rn(f16_bits_to_f32(h45 >> 16), sr[i]);
-            xh[i][6] = __fmul_rn(f16_bits_to_f32(h67 & 0xFFFFu), sr[i]);
-            xh[i][7] = __fmul_rn(f16_bits_to_f32(h67 >> 16), sr[i]);
-        }
+        uint2 vn[8];
+        float srn[8];
+        const int nxt = blk + gridDim.x;
+        if (nxt < n_blocks) load(nxt, vn, srn);
+
+        // pass 1: per-channel amax of the dequantized values
         float ca[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float a = 0.0f;
+        for (int j = 0; j < 8; ++j) ca[j] = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(xh[i][j]));
-            ca[j] = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 16));
+        for (int i = 0; i < 8; ++i) {
+            float2 xr[4];
+            dequant8(v[i], sr[i], xr);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                ca[2 * k] = fmaxf(ca[2 * k], fabsf(xr[k].x));
+                ca[2 * k + 1] = fmaxf(ca[2 * k + 1], fabsf(xr[k].y));
+            }
         }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ca[j] = fmaxf(ca[j], __shfl_xor_sync(0xffffffffu, ca[j], 16));
         if (lane < 16) {
             float4* dst = reinterpret_cast<float4*>(&red[par][warp][nc * 8]);
             dst[0] = make_float4(ca[0], ca[1], ca[2], ca[3]);
             dst[1] = make_float4(ca[4], ca[5], ca[6], ca[7]);
         }
         __syncthreads();
+        if (threadIdx.x < 128) {                 // one scale computation per channel
+            float a = red[par][0][threadIdx.x];
 #pragma unroll
-        for (int ww = 0; ww < 8; ++ww) {
-            const float4* src = reinterpret_cast<const float4*>(&red[par][ww][nc * 8]);
-            const float4 p0 = src[0], p1 = src[1];
-            ca[0] = fmaxf(ca[0], p0.x);
-            ca[1] = fmaxf(ca[1], p0.y);
-            ca[2] = fmaxf(ca[2], p0.z);
-            ca[3] = fmaxf(ca[3], p0.w);
-            ca[4] = fmaxf(ca[4], p1.x);
-            ca[5] = fmaxf(ca[5], p1.y);
-            ca[6] = fmaxf(ca[6], p1.z);
-            ca[7] = fmaxf(ca[7], p1.w);
+            for (int ww = 1; ww < 8; ++ww) a = fmaxf(a, red[par][ww][threadIdx.x]);
+            const GroupScale g = group_scale(a);
+            c_s[par][threadIdx.x] = g.s;
+            c_r[par][threadIdx.x] = g.r;
+            c_mode[par][threadIdx.x] = g.mode;
         }
-        GroupScale g[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = group_scale(ca[j]);
+        __syncthreads();
+
+        // pass 2: dequantize again and quantize with the channel scales
+        float cs[8], cr[8];
+        int all_recip;
+        {
+            const float4* ps = reinterpret_cast<const float4*>(&c_s[par][nc * 8]);
+            const float4* pr = reinterpret_cast<const float4*>(&c_r[par][nc * 8]);
+            const int4* pm = reinterpret_cast<const int4*>(&c_mode[par][nc * 8]);
+            const float4 s0 = ps[0], s1 = ps[1], r0 = pr[0], r1 = pr[1];
+            cs[0] = s0.x; cs[1] = s0.y; cs[2] = s0.z; cs[3] = s0.w;
+            cs[4] = s1.x; cs[5] = s1.y; cs[6] = s1.z; cs[7] = s1.w;
+            cr[0] = r0.x; cr[1] = r0.y; cr[2] = r0.z; cr[3] = r0.w;
+            cr[4] = r1.x; cr[5] = r1.y; cr[6] = r1.z; cr[7] = r1.w;
+            const int4 m0 = pm[0], m1 = pm[1];
+            // all eight channels take the reciprocal path iff the AND of their modes is 1
+            all_recip = (m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w) == 1;
+        }
         uint2 rows[8];
+        if (all_recip) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            rows[i].x = quant_code(xh[i][0], g[0]) | (quant_code(xh[i][1], g[1]) << 8) |
-                        (quant_code(xh[i][2], g[2]) << 16) | (quant_code(xh[i][3], g[3]) << 24);
-            rows[i].y = quant_code(xh[i][4], g[4]) | (quant_code(xh[i][5], g[5]) << 8) |
-                        (quant_code(xh[i][6], g[6]) << 16) | (quant_code(xh[i][7], g[7]) << 24);
+            for (int i = 0; i < 8; ++i) {
+                float2 xr[4];
+                dequant8(v[i], sr[i], xr);
+                uint32_t c[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    c[k] = e4m3_pair(div2_markstein(xr[k], make_float2(cr[2 * k], cr[2 * k + 1]),
+                                                    make_float2(-cs[2 * k], -cs[2 * k + 1])));
+                rows[i] = make_uint2((__byte_perm(c[0], c[1], 0x5410)) | (v[i].x & 0x80808080u),
+                                     (__byte_perm(c[2], c[3], 0x5410)) | (v[i].y & 0x80808080u));
+            }
+        } else {
+            int cm[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) cm[j] = c_mode[par][nc * 8 + j];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float2 xr[4];
+                dequant8(v[i], sr[i], xr);
+                uint32_t cw[2] = {0u, 0u};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t c = quant_div(xr[k].x, cs[2 * k], cm[2 * k]) |
+                                       (quant_div(xr[k].y, cs[2 * k + 1], cm[2 * k + 1]) << 8);
+                    cw[k >> 1] |= c << (16 * (k & 1));
+                }
+                rows[i] = make_uint2(cw[0], cw[1]);
+            }
         }
         uint2 cols[8];
         transpose8x8(rows, cols);
@@ -306,7 +427,12 @@ __global__ void __launch_bounds__(256) k_requant_1x128_to_128x1(const uint8_t* _
         for (int j = 0; j < 8; ++j) stg_v2(qT + (col0 + j) * ldqT + row0, cols[j]);
         if (rb == 0) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sT[(col0 + j) * sTk + static_cast<int64_t>(mb) * sTmb] = g[j].s;
+            for (int j = 0; j < 8; ++j) sT[(col0 + j) * sTk + static_cast<int64_t>(mb) * sTmb] = cs[j];
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = vn[i];
+            sr[i] = srn[i];
         }
     }
 }

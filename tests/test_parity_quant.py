@@ -125,6 +125,42 @@ def test_act_codec_sweep_all_bf16_magnitudes(orc):
     check_act(orc, groups)
 
 
+def exhaustive_ratio_groups(amax_exp):
+    """Groups covering every bf16 (amax, x) significand pair with x = amax * 2^-d
+    scaled, d = 0..21, both signs: element 0 of each group is amax (exponent
+    `amax_exp`), the others are the x values (|x| <= amax), zero padded.  The
+    quotient x / s depends only on the significands and d, so this covers
+    every ratio a bf16 group can produce at this scale."""
+    groups = []
+    for ma in range(128):
+        amax_bits = ((amax_exp + 127) << 7) | ma
+        xs = []
+        for d in range(22):
+            e = amax_exp + 127 - d
+            if e <= 0:
+                break
+            for mx in range(128):
+                if d == 0 and mx > ma:
+                    continue
+                b = (e << 7) | mx
+                xs += [b, b | 0x8000]
+        xs = np.array(xs, np.uint16)
+        pad = (-len(xs)) % 127
+        xs = np.concatenate([xs, np.zeros(pad, np.uint16)]).reshape(-1, 127)
+        groups.append(np.concatenate([np.full((xs.shape[0], 1), amax_bits, np.uint16), xs], axis=1))
+    return np.concatenate(groups)
+
+
+@pytest.mark.parametrize("amax_exp", [0, 60, -60])
+def test_act_exhaustive_bf16_ratios(orc, amax_exp):
+    # every significand pair and exponent gap: the reciprocal-and-correction
+    # quotient must equal the oracle's IEEE division in every case
+    groups = exhaustive_ratio_groups(amax_exp)
+    check_act(orc, groups)
+    n = groups.shape[0] // 4 * 4
+    check_act(orc, groups[:n].reshape(n // 4, 512), scale_layout="row")
+
+
 @pytest.mark.parametrize("M,K", [(1, 128), (3, 256), (77, 384), (1000, 1024)])
 def test_act_ragged_rows_and_strides(orc, M, K):
     x, _ = synth.activation(13, M, K, outlier_frac=0.02)
