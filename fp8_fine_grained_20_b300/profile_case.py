@@ -1,0 +1,126 @@
+"""One kernel of the FP8 path at its benchmark size, for profiler captures.
+
+    python -m fp8_fine_grained_20_b300.profile_case KERNEL [--launches N] [--warmup W]
+
+KERNEL is one of quant_act, quant_w, requant, gemm_fprop, gemm_wgrad,
+grouped_gemm.  The process allocates only what that one call needs (at most
+about 2 GB), fills the bf16 inputs on the device with torch's generator
+(N(0,1) activations with 1% of channels x100, N(0, 0.02^2) weights,
+N(0, 1e-3^2) gradients), quantizes them with the library where the kernel
+takes FP8 operands, then launches the kernel W + N times.  Under
+``ncu -k regex:<name> -s W -c N`` only the last N launches are captured; the
+setup kernels are not.
+
+Kernel names to filter on: k_quant_act_1x128, k_quant_w_128x128,
+k_requant_1x128_to_128x1, k_gemm_blockscaled.
+"""
+import argparse
+import sys
+
+import torch
+
+import fp8_fine_grained_20_b300 as fg
+
+T, CIN, COUT = 8192, 7168, 18432
+G, MOE_K, MOE_N, TOKENS, TOPK, ZIPF = 32, 7168, 2048, 16384, 8, 1.1
+
+
+def _gen(seed):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return g
+
+
+def activation(rows, cols, seed):
+    g = _gen(seed)
+    x = torch.randn((rows, cols), generator=g, device="cuda", dtype=torch.float32)
+    n_out = round(0.01 * cols)
+    idx = torch.randperm(cols, generator=g, device="cuda")[:n_out]
+    x[:, idx] *= 100.0
+    return x.to(torch.bfloat16)
+
+
+def weight(rows, cols, seed, sigma=0.02):
+    g = _gen(seed)
+    return (torch.randn((rows, cols), generator=g, device="cuda", dtype=torch.float32) * sigma).to(torch.bfloat16)
+
+
+def moe_offsets(seed):
+    """Padded per-expert row ranges: Multinomial(16384 x 8, p_g ~ (g+1)^-1.1)."""
+    g = torch.Generator()
+    g.manual_seed(seed)
+    p = torch.arange(1, G + 1, dtype=torch.float64) ** (-ZIPF)
+    picks = torch.multinomial(p / p.sum(), TOKENS * TOPK, replacement=True, generator=g)
+    counts = torch.bincount(picks, minlength=G)
+    padded = (counts + 127) // 128 * 128
+    off = torch.zeros(G + 1, dtype=torch.int64)
+    off[1:] = torch.cumsum(padded, 0)
+    return off.to(torch.int32)
+
+
+def setup(kind):
+    """Returns a closure that launches the kernel once."""
+    if kind == "quant_act":
+        x = activation(T, CIN, 1)
+        q = torch.empty((T, CIN), dtype=torch.uint8, device="cuda")
+        s = torch.empty((CIN // 128, T), dtype=torch.float32, device="cuda").t()
+        return lambda: fg.fp8_quant_act_1x128(x, q, s)
+    if kind == "quant_w":
+        w = weight(CIN, COUT, 2)
+        q = torch.empty((COUT, CIN), dtype=torch.uint8, device="cuda")
+        s = torch.empty((CIN // 128, COUT // 128), dtype=torch.float32, device="cuda")
+        return lambda: fg.fp8_quant_w_128x128(w, q, s)
+    if kind == "requant":
+        q, s = fg.fp8_quant_act_1x128(activation(T, CIN, 3))
+        qT = torch.empty((CIN, T), dtype=torch.uint8, device="cuda")
+        sT = torch.empty((T // 128, CIN), dtype=torch.float32, device="cuda").t()
+        return lambda: fg.fp8_requant_1x128_to_128x1(q, s, qT, sT)
+    if kind == "gemm_fprop":
+        a, sa = fg.fp8_quant_act_1x128(activation(T, CIN, 4))
+        b, sb = fg.fp8_quant_w_128x128(weight(CIN, COUT, 5))
+        c = torch.empty((T, COUT), dtype=torch.bfloat16, device="cuda")
+        return lambda: fg.fp8_gemm_blockscaled(a, sa, b, sb, fg.FP8_SB_BLOCK128x128, c)
+    if kind == "gemm_wgrad":
+        xq, xs = fg.fp8_quant_act_1x128(weight(T, CIN, 6, 1e-3))
+        dq, ds = fg.fp8_quant_act_1x128(weight(T, COUT, 7, 1e-3))
+        a, sa = fg.fp8_requant_1x128_to_128x1(xq, xs)
+        b, sb = fg.fp8_requant_1x128_to_128x1(dq, ds)
+        del xq, xs, dq, ds
+        c = torch.empty((CIN, COUT), dtype=torch.bfloat16, device="cuda")
+        return lambda: fg.fp8_gemm_blockscaled(a, sa, b, sb.t(), fg.FP8_SB_COL128x1, c)
+    if kind == "grouped_gemm":
+        off = moe_offsets(8)
+        rows = int(off[-1])
+        a, sa = fg.fp8_quant_act_1x128(activation(rows, MOE_K, 9))
+        bq = torch.empty((G, MOE_N, MOE_K), dtype=torch.uint8, device="cuda")
+        bs = torch.empty((G, MOE_K // 128, MOE_N // 128), dtype=torch.float32, device="cuda")
+        for e in range(G):
+            fg.fp8_quant_w_128x128(weight(MOE_K, MOE_N, 100 + e), bq[e], bs[e])
+        c = torch.empty((rows, MOE_N), dtype=torch.bfloat16, device="cuda")
+        d_off = off.cuda()
+        return lambda: fg.fp8_grouped_gemm_blockscaled(a, sa, bq, bs, d_off, c)
+    raise SystemExit("unknown kernel %r" % kind)
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("kernel", choices=["quant_act", "quant_w", "requant", "gemm_fprop", "gemm_wgrad",
+                                      "grouped_gemm"])
+    p.add_argument("--launches", type=int, default=1)
+    p.add_argument("--warmup", type=int, default=2)
+    args = p.parse_args(argv)
+    torch.cuda.set_device(0)
+    fg.capi()
+    run = setup(args.kernel)
+    torch.cuda.synchronize()
+    for _ in range(args.warmup + args.launches):
+        run()
+    torch.cuda.synchronize()
+    status = fg.fp8_get_device_status(reset=True)
+    if status != 0:
+        raise SystemExit("device status %d" % status)
+    print("%s: %d launches ok" % (args.kernel, args.warmup + args.launches))
+
+
+if __name__ == "__main__":
+    sys.exit(main())
