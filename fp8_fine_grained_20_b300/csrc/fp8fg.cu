@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -92,24 +93,51 @@ template <int SBK, bool GROUPED>
 fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const uint8_t* B, int64_t ldb,
                          int64_t b_rows, const gemm::Args& args, cudaStream_t stream) {
     static int attr_set[kMaxDevices] = {0};
+    static int max_pairs[kMaxDevices] = {0};
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
-    const int sms = sm_count(dev);
-    if (sms <= 0) return FP8_ERR_CUDA;
     auto kernel = gemm::k_gemm_blockscaled<SBK, GROUPED>;
     const size_t smem = GROUPED ? gemm::SMEM_GROUPED : gemm::SMEM_PLAIN;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(gemm::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (!attr_set[dev]) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess)
             return FP8_ERR_DEVICE;
+        // co-resident CTA pairs: the persistent grid never exceeds this
+        int n = 0;
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count(dev)), 1, 1);
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
+            cudaGetLastError();
+            return FP8_ERR_DEVICE;
+        }
+        max_pairs[dev] = n;
         attr_set[dev] = 1;
     }
     CUtensorMap tmA, tmB;
     if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
-    if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BN)) return FP8_ERR_CUDA;
-    const int64_t tiles = static_cast<int64_t>(args.m_blocks) * args.n_blocks;
-    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
-    kernel<<<grid, gemm::THREADS, smem, stream>>>(tmA, tmB, args);
+    if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BNH)) return FP8_ERR_CUDA;
+    // the grouped pair-row count is known only on the device: bound it by the
+    // padded rows, each expert adding at most one half-empty pair-row
+    int64_t pair_rows = (args.m_blocks + 1) / 2;
+    if (GROUPED) pair_rows = std::min<int64_t>(args.m_blocks, (args.m_blocks + args.G + 1) / 2);
+    const int64_t tiles = pair_rows * args.n_blocks;
+    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(tiles, max_pairs[dev]));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8_ERR_CUDA;
+    }
     return launch_status();
 }
 

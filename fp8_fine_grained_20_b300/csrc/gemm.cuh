@@ -13,17 +13,24 @@
 //
 // B300 design (not the H800 one, where two WGMMA warpgroups alternate
 // between MMA and promotion):
-//   * persistent CTAs (one per SM), 128 x 256 output tiles, grouped raster;
-//   * warp 0: TMA producer -- A (128x128 B) and B (256x128 B) boxes with
-//     128-byte swizzle into a 4-stage shared-memory ring;
-//   * warp 1: MMA issuer -- per K-block, 4 x tcgen05.mma.kind::f8f6f4
-//     (128x256x32) into one of two TMEM partial buffers (2 x 256 columns),
-//     then tcgen05.commit to free the smem stage and publish the partial;
-//   * warp 2: scale loader -- cp.async of the K-block's sA[128] and sB slice
-//     into an 8-slot ring (any scale strides);
-//   * warps 4-11: promotion -- tcgen05.ld of the partial (each warp: its
-//     32 TMEM lanes = rows, one 128-column half), release of the TMEM buffer,
-//     acc += partial * sA * sB in FP32 registers, bf16 store at tile end.
+//   * CTA pairs (clusters of 2 on neighbouring SMs), persistent: each pair
+//     owns 256 x 256 output tiles in a grouped raster.  One tcgen05.mma with
+//     cta_group::2 computes M = 256 (128 rows in each CTA) x N = 256, reading
+//     A from each CTA's own shared memory and half of B's 256 rows from each
+//     CTA, so every SM loads 32 KB per 128-deep K-block instead of 48 KB;
+//   * warp 0 (both CTAs): TMA producer -- this CTA's A box (128 x 128 B) and B
+//     half (128 x 128 B), 128-byte swizzle, 6-stage ring; the transaction
+//     bytes of both CTAs are counted on the even CTA's "full" barrier;
+//   * warp 1 (even CTA): MMA issuer -- per K-block, 4 x tcgen05.mma (K = 32)
+//     into one of two 256-column TMEM partial buffers, then one commit that
+//     frees the smem stage in both CTAs and one that publishes the partial to
+//     both CTAs' promotion warps;
+//   * warp 2 (both CTAs): scale loader -- cp.async of the K-block's 128 row
+//     scales of this CTA and the tile's B scales into an 8-slot ring;
+//   * warps 4-11 (both CTAs): promotion -- tcgen05.ld of this CTA's 128 x 256
+//     partial (each warp: its 32 TMEM lanes = rows, one 128-column half),
+//     release of the TMEM buffer to the even CTA, acc += partial * sA * sB in
+//     FP32 registers, bf16 stores at tile end.
 //   The MMA of K-block kb+1 runs while K-block kb is promoted.
 #pragma once
 
@@ -34,18 +41,22 @@
 namespace fp8fg {
 namespace gemm {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 128;           // rows per CTA
+constexpr int PM = 256;           // rows per CTA pair (MMA M)
+constexpr int BN = 256;           // columns per tile (MMA N)
+constexpr int BNH = BN / 2;       // B rows loaded by each CTA
 constexpr int BK = 128;
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int SSLOTS = 8;
 constexpr int THREADS = 384;
-constexpr int GROUP_M = 16;
+constexpr int PROMO_WARPS = 8;
+constexpr int GROUP_PM = 8;       // pair-rows sharing each n-block sweep of the raster
 constexpr int MAX_GROUPS = 1024;
 constexpr uint32_t A_BYTES = BM * BK;
-constexpr uint32_t B_BYTES = BN * BK;
+constexpr uint32_t B_BYTES = BNH * BK;
+constexpr uint32_t STAGE_TX = 2 * (A_BYTES + B_BYTES);   // both CTAs' loads, counted in the even CTA
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+constexpr uint32_t IDESC = idesc_e4m3_f32(PM, BN);
 
 constexpr int SB_BLOCK = 0;  // sB[kb][n/128]
 constexpr int SB_COL = 1;    // sB[kb][n]
@@ -59,7 +70,7 @@ constexpr int N_BARS = 2 * STAGES + 4 + 2 * SSLOTS + 1;
 constexpr size_t OFF_MISC = OFF_BAR + N_BARS * sizeof(uint64_t);
 constexpr size_t OFF_GOFF = OFF_MISC + 16;
 constexpr size_t SMEM_PLAIN = 1024 + OFF_GOFF;
-constexpr size_t SMEM_GROUPED = 1024 + OFF_GOFF + (MAX_GROUPS + 1) * sizeof(int);
+constexpr size_t SMEM_GROUPED = 1024 + OFF_GOFF + 2 * (MAX_GROUPS + 1) * sizeof(int);
 
 struct Args {
     const float* sA;
@@ -70,7 +81,7 @@ struct Args {
     uint16_t* C;
     int64_t ldc;
     int M, N, K;
-    int m_blocks, n_blocks, k_blocks;
+    int m_blocks, n_blocks, k_blocks;  // n_blocks: 256-column tiles
     int sb_cols;              // number of valid sB columns: N/128 (block) or N (per column)
     const int32_t* offsets;   // grouped only (device)
     int G;
@@ -78,44 +89,54 @@ struct Args {
 
 __device__ const float g_zero_scale = 0.0f;
 
-// Tile t -> (m-block, n-block): GROUP_M consecutive m-blocks share each
-// n-block before moving on, so concurrently running CTAs reuse A and B in L2.
-__device__ __forceinline__ void tile_coords(int t, const Args& p, int& mb, int& nb) {
-    const int span = GROUP_M * p.n_blocks;
+// One pair tile: rows [row0, row0 + 256) of A and C (this CTA's half starts
+// at row0 + 128 * rank), columns [nb * 256, nb * 256 + 256), expert g and the
+// end of that expert's rows (rows at or beyond row_end are computed but not
+// stored).
+struct Tile {
+    int row0, nb, g, row_end;
+};
+
+// Pair-tile index -> (pair-row, n-block): GROUP_PM consecutive pair-rows share
+// each n-block before moving on, so concurrently running pairs reuse A and B
+// in L2.
+__device__ __forceinline__ void raster(int t, int pair_rows, int n_blocks, int& pr, int& nb) {
+    const int span = GROUP_PM * n_blocks;
     const int grp = t / span;
-    const int first = grp * GROUP_M;
-    const int gm = min(GROUP_M, p.m_blocks - first);
+    const int first = grp * GROUP_PM;
+    const int gm = min(GROUP_PM, pair_rows - first);
     const int r = t - grp * span;
-    mb = first + r % gm;
+    pr = first + r % gm;
     nb = r / gm;
 }
 
-// Expert owning the 128-row block mb, or -1 (rows beyond the last expert).
-__device__ __forceinline__ int expert_of_block(int mb, const int* goff, int G) {
-    const int row = mb * BM;
-    if (row >= goff[G]) return -1;
-    int lo = 0, hi = G - 1;  // largest g with goff[g] <= row
+// Expert owning pair-row pr: the largest g with ppre[g] <= pr (ppre[g] = pair
+// rows of experts 0..g-1; empty experts are skipped because their prefix
+// equals the next one's).
+__device__ __forceinline__ int expert_of_pair_row(int pr, const int* ppre, int G) {
+    int lo = 0, hi = G - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (goff[mid] <= row) lo = mid; else hi = mid - 1;
+        if (ppre[mid] <= pr) lo = mid; else hi = mid - 1;
     }
-    return (row >= goff[lo] && row < goff[lo + 1]) ? lo : -1;
+    return lo;
 }
 
 template <bool GROUPED>
-__device__ __forceinline__ bool tile_info(int t, const Args& p, const int* goff, int& mb, int& nb, int& g) {
-    tile_coords(t, p, mb, nb);
+__device__ __forceinline__ Tile tile_at(int t, const Args& p, int pair_rows, const int* goff, const int* ppre) {
+    Tile x;
+    int pr;
+    raster(t, pair_rows, p.n_blocks, pr, x.nb);
     if (!GROUPED) {
-        g = 0;
-        return true;
+        x.g = 0;
+        x.row0 = pr * PM;
+        x.row_end = p.M;
+    } else {
+        x.g = expert_of_pair_row(pr, ppre, p.G);
+        x.row0 = goff[x.g] + (pr - ppre[x.g]) * PM;
+        x.row_end = goff[x.g + 1];
     }
-    g = expert_of_block(mb, goff, p.G);
-    return g >= 0;
-}
-
-__device__ __forceinline__ void signal_abort(volatile int* abort_flag) {
-    *abort_flag = 1;
-    record_status(kStatusTimeout);
+    return x;
 }
 
 template <int SBK, int OFF>
@@ -141,6 +162,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Records the timeout and stops both CTAs of the pair: the flag of this CTA
+// and of its peer are set, so every bounded wait of the pair returns early.
+__device__ __forceinline__ void signal_abort(volatile int* abort_flag, uint32_t peer) {
+    *abort_flag = 1;
+    st_shared_cluster_u32(mapa_shared(smem_addr(const_cast<int*>(abort_flag)), peer), 1u);
+    record_status(kStatusTimeout);
+}
+
+// Launch: clusters of 2 CTAs along x, THREADS threads, SMEM_PLAIN or
+// SMEM_GROUPED bytes of dynamic shared memory, one CTA per SM.
 template <int SBK, bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_blockscaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -152,10 +183,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* sm_sa = reinterpret_cast<float*>(base + OFF_SA);
     float* sm_sb = reinterpret_cast<float*>(base + OFF_SB);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + OFF_BAR);
-    uint64_t* full = bars;
-    uint64_t* empty = full + STAGES;
-    uint64_t* tfull = empty + STAGES;
-    uint64_t* tempty = tfull + 2;
+    uint64_t* full = bars;               // even CTA: both CTAs' TMA bytes of a stage
+    uint64_t* empty = full + STAGES;     // both: stage consumed by the MMAs
+    uint64_t* tfull = empty + STAGES;    // both: partial buffer written
+    uint64_t* tempty = tfull + 2;        // even CTA: partial buffer read by both CTAs
     uint64_t* sfull = tempty + 2;
     uint64_t* sempty = sfull + SSLOTS;
     uint64_t* drain = sempty + SSLOTS;
@@ -163,9 +194,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + OFF_MISC + 4);
     int* groups_ok = reinterpret_cast<int*>(base + OFF_MISC + 8);
     int* goff = reinterpret_cast<int*>(base + OFF_GOFF);
+    int* ppre = goff + (MAX_GROUPS + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const bool leader = rank == 0;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -174,11 +209,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 8);
+            mbar_init(&tempty[i], 2 * PROMO_WARPS);
         }
         for (int i = 0; i < SSLOTS; ++i) {
             mbar_init(&sfull[i], 32);
-            mbar_init(&sempty[i], 8);
+            mbar_init(&sempty[i], PROMO_WARPS);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -191,76 +226,77 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int i = threadIdx.x; i <= p.G; i += THREADS) goff[i] = p.offsets[i];
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
     }
-    tc_fence_before_sync();
     __syncthreads();
-    tc_fence_after_sync();
     if (GROUPED && threadIdx.x == 0) {
-        bool ok = goff[0] >= 0 && goff[p.G] <= p.M;
-        for (int g = 0; g < p.G; ++g) ok = ok && goff[g] <= goff[g + 1] && (goff[g] % BM) == 0;
-        ok = ok && (goff[p.G] % BM) == 0;
+        // validate the offsets and build the prefix of pair-rows per expert
+        bool ok = goff[0] >= 0 && goff[p.G] <= p.M && (goff[p.G] % BM) == 0;
+        int acc = 0;
+        for (int g = 0; g < p.G; ++g) {
+            ok = ok && goff[g] <= goff[g + 1] && (goff[g] % BM) == 0;
+            ppre[g] = acc;
+            if (ok) acc += (goff[g + 1] - goff[g] + PM - 1) / PM;
+        }
+        ppre[p.G] = acc;
         if (!ok) {
             *groups_ok = 0;
             if (blockIdx.x == 0) record_status(kStatusBadGroups);
         }
     }
-    __syncthreads();
+    tc_fence_before_sync();
+    cluster_sync();     // barriers of both CTAs initialised, TMEM allocated, offsets checked
+    tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int num_tiles = (*groups_ok) ? p.m_blocks * p.n_blocks : 0;
+    const int pair_rows = GROUPED ? ppre[p.G] : (p.m_blocks + 1) / 2;
+    const int num_tiles = (*groups_ok) ? pair_rows * p.n_blocks : 0;
+    const int pair = static_cast<int>(cluster_id_x());
+    const int n_pairs = static_cast<int>(n_clusters_x());
 
     if (warp < 4) {
-      regs_decrease<40>();
+      regs_decrease<56>();
       if (warp == 0) {
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
-            uint32_t stage = 0, phase = 0, issued = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                int mb, nb, g;
-                if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
-                const int a_y = mb * BM;
-                const int b_y = g * p.N + nb * BN;
+            uint32_t stage = 0, phase = 0;
+            bool ok = true, issued_any = false;
+            for (int t = pair; ok && t < num_tiles; t += n_pairs) {
+                const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+                const int a_y = tl.row0 + static_cast<int>(rank) * BM;
+                const int b_y = tl.g * p.N + tl.nb * BN + static_cast<int>(rank) * BNH;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
-                        signal_abort(abort_flag);
+                        signal_abort(abort_flag, peer);
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
-                    tma_load_2d(sm_a + stage * A_BYTES, &tmA, &full[stage], kb * BK, a_y);
-                    tma_load_2d(sm_b + stage * B_BYTES, &tmB, &full[stage], kb * BK, b_y);
-                    ++issued;
+                    const uint32_t fbar = mapa_shared(smem_addr(&full[stage]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+                    tma_load_2d_pair(sm_a + stage * A_BYTES, &tmA, fbar, kb * BK, a_y);
+                    tma_load_2d_pair(sm_b + stage * B_BYTES, &tmB, fbar, kb * BK, b_y);
+                    issued_any = true;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            if (!ok) {
-                // drain the loads still in flight before the CTA may exit
-                const uint32_t n = issued < STAGES ? issued : STAGES;
-                for (uint32_t i = 1; i <= n; ++i) {
-                    const uint32_t k = issued - i;
-                    mbar_wait(&full[k % STAGES], (k / STAGES) & 1u, nullptr, kDrainTimeoutNs);
-                }
-            }
+            // after an abort, let the loads still in flight land before the CTA may exit
+            if (!ok && issued_any) spin_ns(100000);
         }
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer ----
-        if (lane == 0) {
+        if (leader && lane == 0) {
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                int mb, nb, g;
-                if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
+            for (int t = pair; ok && t < num_tiles; t += n_pairs) {
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     const uint32_t buf = it & 1u;
                     const uint32_t tph = (it >> 1) & 1u;
-                    if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag) ||
-                        !mbar_wait(&full[stage], phase, abort_flag)) {
-                        signal_abort(abort_flag);
+                    if (!mbar_wait_cluster(&tempty[buf], tph ^ 1u, abort_flag) ||
+                        !mbar_wait_cluster(&full[stage], phase, abort_flag)) {
+                        signal_abort(abort_flag, peer);
                         ok = false;
                         break;
                     }
@@ -271,10 +307,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 32; ++k) {
                         // +32 bytes along K inside the 128-byte swizzle atom: +2 in the (>>4) address field
-                        umma_f8(d, ad + 2u * k, bd + 2u * k, IDESC, k > 0 ? 1u : 0u);
+                        umma_f8_pair(d, ad + 2u * k, bd + 2u * k, IDESC, k > 0 ? 1u : 0u);
                     }
-                    umma_commit(&empty[stage]);
-                    umma_commit(&tfull[buf]);
+                    umma_commit_pair_mc(&empty[stage], 0x3);
+                    umma_commit_pair_mc(&tfull[buf], 0x3);
                     ++it;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -283,21 +319,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             // every MMA this thread issued completes before TMEM is released
-            umma_commit(drain);
+            umma_commit_pair_mc(drain, 0x1);
             mbar_wait(drain, 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     } else if (warp == 2) {
         // ------------------------------------------------ scale loader ----
         uint32_t slot = 0, sph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            int mb, nb, g;
-            if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
-            const float* sa_rows = p.sA + static_cast<int64_t>(mb) * BM * p.sa_sm;
-            const float* sb_base = p.sB + static_cast<int64_t>(g) * p.sb_group_stride;
+        for (int t = pair; ok && t < num_tiles; t += n_pairs) {
+            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            const int r0 = tl.row0 + static_cast<int>(rank) * BM;
+            const float* sb_base = p.sB + static_cast<int64_t>(tl.g) * p.sb_group_stride;
             for (int kb = 0; kb < p.k_blocks; ++kb) {
                 if (!__all_sync(0xffffffffu, mbar_wait(&sempty[slot], sph ^ 1u, abort_flag))) {
-                    if (lane == 0) signal_abort(abort_flag);
+                    if (lane == 0) signal_abort(abort_flag, peer);
                     ok = false;
                     break;
                 }
@@ -305,13 +340,16 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < BM / 32; ++i) {
                     const int r = lane + 32 * i;
-                    cp_async_4(dsa + r, sa_rows + static_cast<int64_t>(r) * p.sa_sm +
-                                            static_cast<int64_t>(kb) * p.sa_skb);
+                    const int row = r0 + r;
+                    const float* src = (row < p.M) ? p.sA + static_cast<int64_t>(row) * p.sa_sm +
+                                                         static_cast<int64_t>(kb) * p.sa_skb
+                                                   : &g_zero_scale;
+                    cp_async_4(dsa + r, src);
                 }
                 float* dsb = sm_sb + slot * BN;
                 if (SBK == SB_BLOCK) {
                     if (lane < BN / 128) {
-                        const int c = nb * (BN / 128) + lane;
+                        const int c = tl.nb * (BN / 128) + lane;
                         const float* src = (c < p.sb_cols) ? sb_base + static_cast<int64_t>(kb) * p.sb_skb +
                                                                  static_cast<int64_t>(c) * p.sb_sn
                                                            : &g_zero_scale;
@@ -321,7 +359,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < BN / 32; ++i) {
                         const int j = lane + 32 * i;
-                        const int c = nb * BN + j;
+                        const int c = tl.nb * BN + j;
                         const float* src = (c < p.sb_cols) ? sb_base + static_cast<int64_t>(kb) * p.sb_skb +
                                                                  static_cast<int64_t>(c) * p.sb_sn
                                                            : &g_zero_scale;
@@ -338,25 +376,24 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("cp.async.wait_all;" ::: "memory");
       }
     } else {
-        regs_increase<232>();
+        regs_increase<224>();
         // ------------------------------------- promotion and epilogue ----
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
-        const int row = quarter * 32 + lane;
+        const int row = quarter * 32 + lane;    // row of this CTA's 128-row half
         uint32_t it = 0, slot = 0, sph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-            int mb, nb, g;
-            if (!tile_info<GROUPED>(t, p, goff, mb, nb, g)) continue;
+        for (int t = pair; ok && t < num_tiles; t += n_pairs) {
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
             for (int kb = 0; kb < p.k_blocks; ++kb) {
                 const uint32_t buf = it & 1u;
                 const uint32_t tph = (it >> 1) & 1u;
-                const bool ready = mbar_wait(&sfull[slot], sph, abort_flag) && mbar_wait(&tfull[buf], tph, abort_flag);
+                const bool ready =
+                    mbar_wait(&sfull[slot], sph, abort_flag) && mbar_wait_cluster(&tfull[buf], tph, abort_flag);
                 if (!__all_sync(0xffffffffu, ready)) {  // warp-uniform: tcgen05.ld is .sync.aligned
-                    if (lane == 0) signal_abort(abort_flag);
+                    if (lane == 0) signal_abort(abort_flag, peer);
                     ok = false;
                     break;
                 }
@@ -379,7 +416,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_wait_ld(r1);
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[buf]);
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&tempty[buf]), 0));  // the even CTA's
                 promote32<SBK, 96>(acc, r1, sc, sa, sbv);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[slot]);
@@ -390,9 +427,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (!ok) break;
-            const int n0 = nb * BN + half * 128;
-            if (n0 < p.N) {
-                uint16_t* crow = p.C + static_cast<int64_t>(mb * BM + row) * p.ldc + n0;
+            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
+            const int n0 = tl.nb * BN + half * 128;
+            if (grow < tl.row_end && n0 < p.N) {
+                uint16_t* crow = p.C + static_cast<int64_t>(grow) * p.ldc + n0;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     uint4 w;
@@ -408,9 +447,10 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    cluster_sync();     // the peer no longer signals this CTA's barriers or reads its TMEM
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc_pair(tmem, TMEM_COLS);
     }
 }
 
