@@ -22,15 +22,16 @@
 //     half (128 x 128 B), 128-byte swizzle, 6-stage ring; the transaction
 //     bytes of both CTAs are counted on the even CTA's "full" barrier;
 //   * warp 1 (even CTA): MMA issuer -- per K-block, 4 x tcgen05.mma (K = 32)
-//     into one of two 256-column TMEM partial buffers, then one commit that
-//     frees the smem stage in both CTAs and one that publishes the partial to
-//     both CTAs' promotion warps;
+//     into one of two 256-column TMEM partial buffers, then one commit to the
+//     stage's "done" barrier in both CTAs, which both frees the smem stage for
+//     the producers and publishes the partial to the promotion warps (the
+//     issuing thread is the scarce resource: one commit per K-block, not two);
 //   * warp 2 (both CTAs): scale loader -- cp.async of the K-block's 128 row
 //     scales of this CTA and the tile's B scales into an 8-slot ring;
 //   * warps 4-11 (both CTAs): promotion -- tcgen05.ld of this CTA's 128 x 256
 //     partial (each warp: its 32 TMEM lanes = rows, one 128-column half),
 //     release of the TMEM buffer to the even CTA, acc += partial * sA * sB in
-//     FP32 registers, bf16 stores at tile end.
+//     FP32 registers with packed FP32x2 FMAs, bf16 stores at tile end.
 //   The MMA of K-block kb+1 runs while K-block kb is promoted.
 #pragma once
 
@@ -66,7 +67,7 @@ constexpr size_t OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr size_t OFF_SA = OFF_B + STAGES * B_BYTES;
 constexpr size_t OFF_SB = OFF_SA + SSLOTS * BM * sizeof(float);
 constexpr size_t OFF_BAR = OFF_SB + SSLOTS * BN * sizeof(float);
-constexpr int N_BARS = 2 * STAGES + 4 + 2 * SSLOTS + 1;
+constexpr int N_BARS = 2 * STAGES + 2 + 2 * SSLOTS + 1;
 constexpr size_t OFF_MISC = OFF_BAR + N_BARS * sizeof(uint64_t);
 constexpr size_t OFF_GOFF = OFF_MISC + 16;
 constexpr size_t SMEM_PLAIN = 1024 + OFF_GOFF;
@@ -143,16 +144,29 @@ template <int SBK, int OFF>
 __device__ __forceinline__ void promote32(float (&acc)[128], const uint32_t (&r)[32], float sc, float sa,
                                           const float* sbv) {
     if (SBK == SB_BLOCK) {
+        const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) acc[OFF + j] = fmaf(__uint_as_float(r[j]), sc, acc[OFF + j]);
+        for (int j = 0; j < 32; j += 2) {
+            float2 a = make_float2(acc[OFF + j], acc[OFF + j + 1]);
+            a = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), sc2, a);
+            acc[OFF + j] = a.x;
+            acc[OFF + j + 1] = a.y;
+        }
     } else {
+        const float2 sa2 = make_float2(sa, sa);
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
             const float4 b = *reinterpret_cast<const float4*>(sbv + OFF + j);
-            acc[OFF + j + 0] = fmaf(__uint_as_float(r[j + 0]), __fmul_rn(sa, b.x), acc[OFF + j + 0]);
-            acc[OFF + j + 1] = fmaf(__uint_as_float(r[j + 1]), __fmul_rn(sa, b.y), acc[OFF + j + 1]);
-            acc[OFF + j + 2] = fmaf(__uint_as_float(r[j + 2]), __fmul_rn(sa, b.z), acc[OFF + j + 2]);
-            acc[OFF + j + 3] = fmaf(__uint_as_float(r[j + 3]), __fmul_rn(sa, b.w), acc[OFF + j + 3]);
+            const float2 w0 = __fmul2_rn(sa2, make_float2(b.x, b.y));
+            const float2 w1 = __fmul2_rn(sa2, make_float2(b.z, b.w));
+            float2 a0 = make_float2(acc[OFF + j], acc[OFF + j + 1]);
+            float2 a1 = make_float2(acc[OFF + j + 2], acc[OFF + j + 3]);
+            a0 = __ffma2_rn(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), w0, a0);
+            a1 = __ffma2_rn(make_float2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])), w1, a1);
+            acc[OFF + j] = a0.x;
+            acc[OFF + j + 1] = a0.y;
+            acc[OFF + j + 2] = a1.x;
+            acc[OFF + j + 3] = a1.y;
         }
     }
 }
@@ -184,9 +198,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     float* sm_sb = reinterpret_cast<float*>(base + OFF_SB);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + OFF_BAR);
     uint64_t* full = bars;               // even CTA: both CTAs' TMA bytes of a stage
-    uint64_t* empty = full + STAGES;     // both: stage consumed by the MMAs
-    uint64_t* tfull = empty + STAGES;    // both: partial buffer written
-    uint64_t* tempty = tfull + 2;        // even CTA: partial buffer read by both CTAs
+    uint64_t* done = full + STAGES;      // both: the K-block held by a stage is multiplied
+                                         // (stage free for TMA, partial ready for promotion)
+    uint64_t* tempty = done + STAGES;    // even CTA: partial buffer read by both CTAs
     uint64_t* sfull = tempty + 2;
     uint64_t* sempty = sfull + SSLOTS;
     uint64_t* drain = sempty + SSLOTS;
@@ -205,12 +219,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+            mbar_init(&done[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 2 * PROMO_WARPS);
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(&tempty[i], 2 * PROMO_WARPS);
         for (int i = 0; i < SSLOTS; ++i) {
             mbar_init(&sfull[i], 32);
             mbar_init(&sempty[i], PROMO_WARPS);
@@ -266,7 +277,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int a_y = tl.row0 + static_cast<int>(rank) * BM;
                 const int b_y = tl.g * p.N + tl.nb * BN + static_cast<int>(rank) * BNH;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&done[stage], phase ^ 1u, abort_flag)) {
                         signal_abort(abort_flag, peer);
                         ok = false;
                         break;
@@ -294,8 +305,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     const uint32_t buf = it & 1u;
                     const uint32_t tph = (it >> 1) & 1u;
-                    if (!mbar_wait_cluster(&tempty[buf], tph ^ 1u, abort_flag) ||
-                        !mbar_wait_cluster(&full[stage], phase, abort_flag)) {
+                    if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag) ||
+                        !mbar_wait(&full[stage], phase, abort_flag)) {
                         signal_abort(abort_flag, peer);
                         ok = false;
                         break;
@@ -309,8 +320,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // +32 bytes along K inside the 128-byte swizzle atom: +2 in the (>>4) address field
                         umma_f8_pair(d, ad + 2u * k, bd + 2u * k, IDESC, k > 0 ? 1u : 0u);
                     }
-                    umma_commit_pair_mc(&empty[stage], 0x3);
-                    umma_commit_pair_mc(&tfull[buf], 0x3);
+                    umma_commit_pair_mc(&done[stage], 0x3);
                     ++it;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -381,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
         const int row = quarter * 32 + lane;    // row of this CTA's 128-row half
-        uint32_t it = 0, slot = 0, sph = 0;
+        uint32_t it = 0, slot = 0, sph = 0, stage = 0, phase = 0;
         bool ok = true;
         for (int t = pair; ok && t < num_tiles; t += n_pairs) {
             float acc[128];
@@ -389,9 +399,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
             for (int kb = 0; kb < p.k_blocks; ++kb) {
                 const uint32_t buf = it & 1u;
-                const uint32_t tph = (it >> 1) & 1u;
-                const bool ready =
-                    mbar_wait(&sfull[slot], sph, abort_flag) && mbar_wait_cluster(&tfull[buf], tph, abort_flag);
+                const bool ready = mbar_wait(&sfull[slot], sph, abort_flag) &&
+                                   mbar_wait(&done[stage], phase, abort_flag);
                 if (!__all_sync(0xffffffffu, ready)) {  // warp-uniform: tcgen05.ld is .sync.aligned
                     if (lane == 0) signal_abort(abort_flag, peer);
                     ok = false;
@@ -424,6 +433,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (++slot == SSLOTS) {
                     slot = 0;
                     sph ^= 1u;
+                }
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
             if (!ok) break;

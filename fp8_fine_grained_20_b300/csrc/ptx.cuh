@@ -62,7 +62,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -70,8 +70,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for the completion of the phase with the given parity.  Returns false
-// when `*abort` becomes non-zero or when the bound expires.
+// Wait for the completion of the phase with the given parity (the barrier may
+// be arrived on by this CTA, by the peer CTA of a pair or by tensor-core
+// commits).  try_wait suspends the thread until the phase completes or the
+// hinted time passes, so waiting warps take few issue slots from the warps
+// that work.  Returns false when `*abort` becomes non-zero or when the bound
+// expires.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                                           uint64_t timeout_ns = kWaitTimeoutNs) {
     const uint32_t a = smem_addr(bar);
@@ -130,35 +134,6 @@ __device__ __forceinline__ void st_shared_cluster_u32(uint32_t cluster_addr, uin
 // would fence all of the thread's memory operations at GPU level.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// mbar_wait for barriers that the peer CTA (or the even CTA's tensor-core
-// commits) arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                                  uint64_t timeout_ns = kWaitTimeoutNs) {
-    const uint32_t a = smem_addr(bar);
-    if (mbar_try_wait_cluster(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
-        if (mbar_try_wait_cluster(a, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (abort != nullptr && *abort) return false;
-            if (global_timer_ns() - t0 > timeout_ns) return false;
-        }
-    }
-    return false;
 }
 
 // Spin for about `ns` nanoseconds (bounded by the global timer).
