@@ -13,6 +13,8 @@ Functions (same names as the C entry points):
   sunipension.com post 314414, Figure 7(a))
 * ``fp8_quant_w_128x128(w)`` -- bf16 [K, N] -> (codes uint8 [N, K] (K-major)
   or [K, N], scales float32 [K/128, N/128])   (128x128 blocks, same figure)
+* ``fp8_quant_w_128x128_batched(w)`` -- the same for G weights [G, K, N] in one
+  launch (the experts of an MoE layer)
 * ``fp8_requant_1x128_to_128x1(q, s)`` -- (uint8 [M, K], [M, K/128]) ->
   (uint8 [K, M], float32 logical [K, M/128])   (backward-pass retiling, same page)
 * ``fp8_gemm_blockscaled(A, sA, B, sB, sb_kind)`` -- bf16 [M, N]; FP32
@@ -33,7 +35,8 @@ import torch
 
 __all__ = [
     "FP8Error", "capi", "library_path",
-    "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_requant_1x128_to_128x1",
+    "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_batched",
+    "fp8_requant_1x128_to_128x1",
     "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled",
     "fp8_get_device_status", "fp8_status_string",
     "FP8_KMAJOR_NK", "FP8_ROWMAJOR_KN", "FP8_SB_BLOCK128x128", "FP8_SB_COL128x1",
@@ -58,6 +61,8 @@ _i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
 _SIGNATURES = {
     "fp8_quant_act_1x128": [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp],
     "fp8_quant_w_128x128": [_vp, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _i64, _vp],
+    "fp8_quant_w_128x128_batched": [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _int, _vp, _i64, _i64,
+                                    _i64, _vp],
     "fp8_requant_1x128_to_128x1": [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64,
                                    _vp],
     "fp8_gemm_blockscaled": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
@@ -177,6 +182,32 @@ def fp8_quant_w_128x128(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, stream=Non
     _check(capi().fp8_quant_w_128x128(_ptr(w), K, N, w.stride(0), _ptr(q), q.stride(0), int(q_layout),
                                       _ptr(s), s.stride(0), s.stride(1), _stream(stream)),
            "fp8_quant_w_128x128")
+    return q, s
+
+
+def fp8_quant_w_128x128_batched(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, stream=None):
+    """128x128 quantization of G weights in one launch.  w: bf16 [G, K, N]
+    (each weight row-major, any expert stride).  Returns (q, s) with q uint8
+    [G, N, K] for FP8_KMAJOR_NK (default) or [G, K, N] for FP8_ROWMAJOR_KN and
+    s float32 [G, K/128, N/128]."""
+    _need_cuda(w)
+    if w.dim() != 3 or w.stride(2) != 1:
+        raise ValueError("w must be a 3-D tensor with unit stride along its last dimension")
+    if w.dtype != torch.bfloat16:
+        raise TypeError("w must be bfloat16")
+    G, K, N = w.shape
+    if q is None:
+        shape = (G, N, K) if q_layout == FP8_KMAJOR_NK else (G, K, N)
+        q = torch.empty(shape, dtype=torch.uint8, device=w.device)
+    if s is None:
+        s = torch.empty((G, K // 128, N // 128), dtype=torch.float32, device=w.device)
+    _need_cuda(q, s)
+    if q.dim() != 3 or q.stride(2) != 1 or s.dim() != 3:
+        raise ValueError("q must be 3-D with unit inner stride and s 3-D")
+    _check(capi().fp8_quant_w_128x128_batched(_ptr(w), G, K, N, w.stride(1), w.stride(0), _ptr(q), q.stride(1),
+                                              q.stride(0), int(q_layout), _ptr(s), s.stride(1), s.stride(2),
+                                              s.stride(0), _stream(stream)),
+           "fp8_quant_w_128x128_batched")
     return q, s
 
 

@@ -89,6 +89,32 @@ bool make_kmajor_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
     return r == CUDA_SUCCESS;
 }
 
+// Tiled map without swizzling over a row-major tensor of `rank` dims (dims[0]
+// innermost, strides in bytes for dims 1..rank-1), boxes of box[] elements.
+bool make_plain_map(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, int rank, const cuuint64_t* dims,
+                    const cuuint64_t* strides, const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r = fn(map, dt, static_cast<cuuint32_t>(rank), const_cast<void*>(ptr), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Dynamic shared memory above 48 KB, once per kernel and device.
+template <typename K>
+bool allow_smem(K kernel, size_t bytes, int dev, int* done) {
+    if (dev < 0 || dev >= kMaxDevices) return false;
+    if (!done[dev]) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+            cudaSuccess)
+            return false;
+        done[dev] = 1;
+    }
+    return true;
+}
+
 template <int SBK, bool GROUPED>
 fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const uint8_t* B, int64_t ldb,
                          int64_t b_rows, const gemm::Args& args, cudaStream_t stream) {
@@ -201,29 +227,58 @@ fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_
     return launch_status();
 }
 
-fp8_status_t fp8_quant_w_128x128(const uint16_t* w, int64_t K, int64_t N, int64_t ldw, uint8_t* q, int64_t ldq,
-                                 int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb, void* stream) {
-    if (K < 0 || N < 0 || K % 128 || N % 128) return FP8_ERR_SHAPE;
+fp8_status_t fp8_quant_w_128x128_batched(const uint16_t* w, int64_t G, int64_t K, int64_t N, int64_t ldw,
+                                         int64_t w_batch_stride, uint8_t* q, int64_t ldq, int64_t q_batch_stride,
+                                         int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb,
+                                         int64_t s_batch_stride, void* stream) {
+    if (G < 0 || K < 0 || N < 0 || K % 128 || N % 128) return FP8_ERR_SHAPE;
     if (q_layout != FP8_KMAJOR_NK && q_layout != FP8_ROWMAJOR_KN) return FP8_ERR_ARG;
-    if (K == 0 || N == 0) return FP8_OK;
+    if (G == 0 || K == 0 || N == 0) return FP8_OK;
     if (!w || !q || !s) return FP8_ERR_NULL;
-    const int64_t q_min_ld = (q_layout == FP8_KMAJOR_NK) ? K : N;
+    const bool kmajor = q_layout == FP8_KMAJOR_NK;
+    const int64_t q_min_ld = kmajor ? K : N;
     if (ldw < N || ldq < q_min_ld || s_stride_kb < 0 || s_stride_nb < 0) return FP8_ERR_ARG;
-    if (!aligned16(w) || !aligned16(q) || (ldw * 2) % 16 || ldq % 16 || (reinterpret_cast<uintptr_t>(s) & 3u))
+    if (G > 1 && (w_batch_stride < K * ldw || q_batch_stride < (kmajor ? N : K) * ldq || s_batch_stride < 0))
+        return FP8_ERR_ARG;
+    if (!aligned16(w) || !aligned16(q) || (ldw * 2) % 16 || ldq % 16 || (reinterpret_cast<uintptr_t>(s) & 3u) ||
+        (G > 1 && ((w_batch_stride * 2) % 16 || q_batch_stride % 16)))
         return FP8_ERR_ALIGN;
     const int64_t KB = K / 128, NB = N / 128;
-    if (KB * NB > INT32_MAX) return FP8_ERR_SHAPE;
-    static int occ[kMaxDevices] = {0};
+    if (G * KB * NB > INT32_MAX || K > INT32_MAX || N > INT32_MAX) return FP8_ERR_SHAPE;
+    static int smem_ok[kMaxDevices] = {0};
     const int dev = current_device();
     const int sms = sm_count(dev);
     if (sms <= 0) return FP8_ERR_CUDA;
-    const int per_sm = blocks_per_sm(k_quant_w_128x128, 256, dev, occ);
-    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
-    const int grid = static_cast<int>(KB * NB < cap ? KB * NB : cap);
-    k_quant_w_128x128<<<grid, 256, 0, as_stream(stream)>>>(w, static_cast<int>(KB), static_cast<int>(NB), ldw, q,
-                                                            ldq, q_layout == FP8_KMAJOR_NK ? 1 : 0, s,
-                                                            s_stride_kb, s_stride_nb);
+    if (!allow_smem(k_quant_w_128x128, WQ_SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
+    CUtensorMap tm;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(G)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldw * 2),
+                                   static_cast<cuuint64_t>((G > 1 ? w_batch_stride : K * ldw) * 2)};
+    const cuuint32_t box[3] = {128u, 128u, 1u};
+    if (!make_plain_map(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, w, 3, dims, strides, box)) return FP8_ERR_CUDA;
+    QuantWArgs a{};
+    a.q = q;
+    a.ldq = ldq;
+    a.q_gstride = q_batch_stride;
+    a.s = s;
+    a.sskb = s_stride_kb;
+    a.ssnb = s_stride_nb;
+    a.s_gstride = s_batch_stride;
+    a.G = static_cast<int>(G);
+    a.KB = static_cast<int>(KB);
+    a.NB = static_cast<int>(NB);
+    a.kmajor = kmajor ? 1 : 0;
+    const int64_t blocks = G * KB * NB;
+    const int64_t cap = 2 * static_cast<int64_t>(sms);
+    const int grid = static_cast<int>(blocks < cap ? blocks : cap);
+    k_quant_w_128x128<<<grid, WQ_THREADS, WQ_SMEM, as_stream(stream)>>>(tm, a);
     return launch_status();
+}
+
+fp8_status_t fp8_quant_w_128x128(const uint16_t* w, int64_t K, int64_t N, int64_t ldw, uint8_t* q, int64_t ldq,
+                                 int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb, void* stream) {
+    return fp8_quant_w_128x128_batched(w, 1, K, N, ldw, 0, q, ldq, 0, q_layout, s, s_stride_kb, s_stride_nb, 0,
+                                       stream);
 }
 
 fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, int64_t ldq, const float* s,
@@ -238,17 +293,31 @@ fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, 
         (reinterpret_cast<uintptr_t>(sT) & 3u))
         return FP8_ERR_ALIGN;
     const int64_t MB = M / 128, KB = K / 128;
-    if (MB * KB > INT32_MAX) return FP8_ERR_SHAPE;
-    static int occ[kMaxDevices] = {0};
+    if (MB * KB > INT32_MAX || M > INT32_MAX || K > INT32_MAX) return FP8_ERR_SHAPE;
+    static int smem_ok[kMaxDevices] = {0};
     const int dev = current_device();
     const int sms = sm_count(dev);
     if (sms <= 0) return FP8_ERR_CUDA;
-    const int per_sm = blocks_per_sm(k_requant_1x128_to_128x1, 256, dev, occ);
-    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    if (!allow_smem(k_requant_1x128_to_128x1, RQ_SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
+    CUtensorMap tm;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldq)};
+    const cuuint32_t box[2] = {128u, 128u};
+    if (!make_plain_map(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dims, strides, box)) return FP8_ERR_CUDA;
+    RequantArgs a{};
+    a.s = s;
+    a.ssm = s_stride_m;
+    a.sskb = s_stride_kb;
+    a.qT = qT;
+    a.ldqT = ldqT;
+    a.sT = sT;
+    a.sTk = sT_stride_k;
+    a.sTmb = sT_stride_mb;
+    a.MB = static_cast<int>(MB);
+    a.KB = static_cast<int>(KB);
+    const int64_t cap = 2 * static_cast<int64_t>(sms);
     const int grid = static_cast<int>(MB * KB < cap ? MB * KB : cap);
-    k_requant_1x128_to_128x1<<<grid, 256, 0, as_stream(stream)>>>(q, static_cast<int>(MB), static_cast<int>(KB),
-                                                                   ldq, s, s_stride_m, s_stride_kb, qT, ldqT, sT,
-                                                                   sT_stride_k, sT_stride_mb);
+    k_requant_1x128_to_128x1<<<grid, RQ_THREADS, RQ_SMEM, as_stream(stream)>>>(tm, a);
     return launch_status();
 }
 

@@ -121,8 +121,8 @@ __device__ __forceinline__ uint2 quant8_bf16(const uint4& v, const GroupScale& g
     return make_uint2(o[0], o[1]);
 }
 
-// Transpose an 8x8 byte matrix held as rows (r[i].x = bytes 0-3, r[i].y =
-// bytes 4-7 of row i) into columns (c[j] = bytes of column j, rows 0-7).
+// Transpose a 4x4 byte matrix held as rows a0..a3 (byte j of a_i = element
+// (i, j)) into columns c0..c3 (byte i of c_j = element (i, j)).
 __device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t& c0,
                                              uint32_t& c1, uint32_t& c2, uint32_t& c3) {
     const uint32_t t0 = __byte_perm(a0, a1, 0x5140);  // a0.b0 a1.b0 a0.b1 a1.b1
@@ -135,14 +135,39 @@ __device__ __forceinline__ void transpose4x4(uint32_t a0, uint32_t a1, uint32_t 
     c3 = __byte_perm(t1, t3, 0x7632);
 }
 
+// 8x8 byte matrix: rows r[i] (.x = bytes 0-3, .y = bytes 4-7 of row i) ->
+// columns c[j] (.x = rows 0-3, .y = rows 4-7 of column j).
 __device__ __forceinline__ void transpose8x8(const uint2 (&r)[8], uint2 (&c)[8]) {
     uint32_t lo[8], hi[8];
-    transpose4x4(r[0].x, r[1].x, r[2].x, r[3].x, lo[0], lo[1], lo[2], lo[3]);  // rows 0-3, cols 0-3
-    transpose4x4(r[4].x, r[5].x, r[6].x, r[7].x, hi[0], hi[1], hi[2], hi[3]);  // rows 4-7, cols 0-3
-    transpose4x4(r[0].y, r[1].y, r[2].y, r[3].y, lo[4], lo[5], lo[6], lo[7]);  // rows 0-3, cols 4-7
-    transpose4x4(r[4].y, r[5].y, r[6].y, r[7].y, hi[4], hi[5], hi[6], hi[7]);  // rows 4-7, cols 4-7
+    transpose4x4(r[0].x, r[1].x, r[2].x, r[3].x, lo[0], lo[1], lo[2], lo[3]);
+    transpose4x4(r[4].x, r[5].x, r[6].x, r[7].x, hi[0], hi[1], hi[2], hi[3]);
+    transpose4x4(r[0].y, r[1].y, r[2].y, r[3].y, lo[4], lo[5], lo[6], lo[7]);
+    transpose4x4(r[4].y, r[5].y, r[6].y, r[7].y, hi[4], hi[5], hi[6], hi[7]);
 #pragma unroll
     for (int j = 0; j < 8; ++j) c[j] = make_uint2(lo[j], hi[j]);
+}
+
+// Output staging for the transposed (128 rows x 128 bytes) tiles: row i
+// starts at i*128 + 16*(i >> SHIFT), a shift that grows by one 16-byte bank
+// group every 2^SHIFT rows, so the writers of one warp (same 16-byte column,
+// rows 2^SHIFT apart) hit different bank groups, and rows never overlap.
+template <int SHIFT>
+__device__ __forceinline__ uint32_t stage_row(int i) {
+    return static_cast<uint32_t>(i * 128 + 16 * (i >> SHIFT));
+}
+template <int SHIFT>
+constexpr uint32_t stage_bytes() {
+    return 127 * 128 + 16 * (127 >> SHIFT) + 128;
+}
+
+__device__ __forceinline__ void sts_v2(void* p, uint2 v) {
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void sts_v4(void* p, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
 }
 
 // ------------------------------------------------- 1x128 activations ----
@@ -209,232 +234,326 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
 
 // ------------------------------------------------------ 128x128 weights ----
 //
-// One CTA (256 threads) per 128x128 block per iteration.  Thread (warp w,
-// lane l) holds rows 8*rb .. 8*rb+7 (rb = 2w + l/16) and columns 8*(l%16) ..
-// +7 of the block: eight 16-byte loads, each row segment read by 16
-// consecutive lanes; the next block's loads are issued before the current
-// block is processed.  The block amax is reduced through shared memory; the
-// K-major output layout is produced by an in-register 8x8 byte transpose.
-__global__ void __launch_bounds__(256, 2) k_quant_w_128x128(const uint16_t* __restrict__ w, int KB, int NB,
-                                                            int64_t ldw, uint8_t* __restrict__ q, int64_t ldq,
-                                                            int kmajor, float* __restrict__ s, int64_t sskb,
-                                                            int64_t ssnb) {
-    __shared__ float red[2][8];
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int nc = lane & 15;
-    const int rb = warp * 2 + (lane >> 4);
-    const int n_blocks = KB * NB;
-    int blk = blockIdx.x;
-    if (blk >= n_blocks) return;
-    uint4 v[8];
-    auto load = [&](int b, uint4 (&dst)[8]) {
-        const int kb_ = b / NB;
-        const int nb_ = b - kb_ * NB;
-        const uint16_t* src = w + (static_cast<int64_t>(kb_) * 128 + rb * 8) * ldw + nb_ * 128 + nc * 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = ldg_nc_v4(src + i * ldw);
+// Persistent CTAs (two per SM), each owning every gridDim.x-th 128x128 block
+// of a batch of weights (expert g, K-block kb, N-block nb).  TMA brings the
+// 32 KB bf16 blocks into a WQ_STAGES-deep shared-memory ring, so that many
+// blocks per CTA are in flight while one is processed.  A thread owns an 8x8
+// sub-block (rows k = 8rb.., columns n = 8nc..): eight 16-byte shared loads
+// (a warp reads two full 256-byte rows per load).  The block amax is reduced
+// through shared memory; as soon as every thread holds its sub-block the
+// stage is refilled.  Row-major output q[g][k][n]: 8-byte stores, 16 lanes per
+// 128-byte output row.  K-major output q[g][n][k]: an in-register 8x8 byte
+// transpose, then the 128 x 128-byte tile is staged in shared memory (rows
+// skewed by a bank group every 8 rows, so a warp's writes do not conflict)
+// and copied out with 16-byte stores, 8 lanes per 128-byte output row.
+constexpr int WQ_STAGES = 3;
+constexpr int WQ_THREADS = 256;
+constexpr uint32_t WQ_TILE_BYTES = 128 * 128 * 2;
+constexpr uint32_t WQ_STAGE_OUT = 16640;   // >= stage_bytes<3>(), multiple of 128
+static_assert(WQ_STAGE_OUT >= stage_bytes<3>() && WQ_STAGE_OUT % 128 == 0, "weight staging tile");
+constexpr size_t WQ_SMEM = 128 + WQ_STAGES * WQ_TILE_BYTES + WQ_STAGE_OUT + WQ_STAGES * 8 + 8 * 4;
+
+struct QuantWArgs {
+    uint8_t* q;
+    int64_t ldq, q_gstride;   // row stride and expert stride of the codes (elements)
+    float* s;
+    int64_t sskb, ssnb, s_gstride;
+    int G, KB, NB;
+    int kmajor;
+};
+
+__device__ __forceinline__ uint4 lds_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_addr(p)));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)));
+    return v;
+}
+
+__global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_constant__ CUtensorMap tmW,
+                                                                   const QuantWArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t* tiles = base;
+    uint8_t* out = base + WQ_STAGES * WQ_TILE_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(out + WQ_STAGE_OUT);
+    float* red = reinterpret_cast<float*>(full + WQ_STAGES);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int rb = 2 * warp + (lane >> 4);    // rows 8 rb .. 8 rb + 7 of the block
+    const int nc = lane & 15;                 // columns 8 nc .. 8 nc + 7
+    const int per_g = a.KB * a.NB;
+    const int total = a.G * per_g;
+
+    auto issue = [&](int stage, int blk) {
+        const int g = blk / per_g;
+        const int r = blk - g * per_g;
+        const int kb = r / a.NB;
+        const int nb = r - kb * a.NB;
+        mbar_arrive_expect_tx(&full[stage], WQ_TILE_BYTES);
+        tma_load_3d(tiles + stage * WQ_TILE_BYTES, &tmW, &full[stage], nb * 128, kb * 128, g);
     };
-    load(blk, v);
-    int par = 0;
-    for (; blk < n_blocks; blk += gridDim.x, par ^= 1) {
-        const int kb = blk / NB;
-        const int nb = blk - kb * NB;
-        const int64_t row0 = static_cast<int64_t>(kb) * 128 + rb * 8;
-        uint4 vn[8];
-        const int nxt = blk + gridDim.x;
-        if (nxt < n_blocks) load(nxt, vn);
+    if (tid == 0) {
+        for (int i = 0; i < WQ_STAGES; ++i) mbar_init(&full[i], 1);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmW);
+        for (int i = 0; i < WQ_STAGES; ++i) {
+            const int blk = blockIdx.x + i * gridDim.x;
+            if (blk < total) issue(i, blk);
+        }
+    }
+    __syncthreads();
+
+    bool ok = true;
+    for (int i = 0;; ++i) {
+        const int blk = blockIdx.x + i * gridDim.x;
+        if (blk >= total) break;
+        const int stage = i % WQ_STAGES;
+        if (!__syncthreads_and(mbar_wait(&full[stage], (i / WQ_STAGES) & 1u, nullptr))) {
+            if (tid == 0) record_status(kStatusTimeout);
+            ok = false;
+            break;
+        }
+        const int g = blk / per_g;
+        const int r = blk - g * per_g;
+        const int kb = r / a.NB;
+        const int nb = r - kb * a.NB;
+        const uint8_t* tile = tiles + stage * WQ_TILE_BYTES;   // bf16 [128 k][128 n], 256-byte rows
+
+        uint4 v[8];
         uint32_t h = 0u;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) h = umax16x2(h, absmax_bf16x8(v[i]));
-        float a = hmax_bf16x2_to_f32(h);
+        for (int j = 0; j < 8; ++j) {
+            v[j] = lds_v4(tile + (8 * rb + j) * 256 + nc * 16);
+            h = umax16x2(h, absmax_bf16x8(v[j]));
+        }
+        float am = hmax_bf16x2_to_f32(h);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (lane == 0) red[par][warp] = a;
-        __syncthreads();
-        a = red[par][0];
+        for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        if (lane == 0) red[warp] = am;
+        __syncthreads();   // A: red[] complete; every thread holds its sub-block, the stage is free
+        if (tid == 0) {
+            const int nxt = blk + WQ_STAGES * gridDim.x;
+            if (nxt < total) issue(stage, nxt);
+        }
+        am = red[0];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) a = fmaxf(a, red[par][i]);
-        const GroupScale g = group_scale(a);
+        for (int k = 1; k < 8; ++k) am = fmaxf(am, red[k]);
+        const GroupScale gs = group_scale(am);
+        if (tid == 0)
+            a.s[static_cast<int64_t>(g) * a.s_gstride + static_cast<int64_t>(kb) * a.sskb +
+                static_cast<int64_t>(nb) * a.ssnb] = gs.s;
+
         uint2 rows[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) rows[i] = quant8_bf16(v[i], g);
-        if (!kmajor) {
+        for (int j = 0; j < 8; ++j) rows[j] = quant8_bf16(v[j], gs);
+        uint8_t* qg = a.q + static_cast<int64_t>(g) * a.q_gstride;
+        if (!a.kmajor) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) stg_v2(q + (row0 + i) * ldq + nb * 128 + nc * 8, rows[i]);
+            for (int j = 0; j < 8; ++j)
+                stg_v2(qg + static_cast<int64_t>(kb * 128 + 8 * rb + j) * a.ldq + nb * 128 + 8 * nc, rows[j]);
+            __syncthreads();   // B: red[] may be rewritten by the next block
         } else {
             uint2 cols[8];
             transpose8x8(rows, cols);
-            const int64_t n0 = static_cast<int64_t>(nb) * 128 + nc * 8;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) stg_v2(q + (n0 + j) * ldq + row0, cols[j]);
+            for (int j = 0; j < 8; ++j) sts_v2(out + stage_row<3>(8 * nc + j) + 8 * rb, cols[j]);
+            __syncthreads();   // B: the staged tile is complete
+            uint8_t* dst = qg + static_cast<int64_t>(nb * 128) * a.ldq + kb * 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int id = tid + WQ_THREADS * u;    // 128 rows x 8 chunks of 16 bytes
+                const int row = id >> 3, ch = id & 7;
+                stg_v4(dst + static_cast<int64_t>(row) * a.ldq + 16 * ch, lds_v4(out + stage_row<3>(row) + 16 * ch));
+            }
         }
-        if (threadIdx.x == 0) s[static_cast<int64_t>(kb) * sskb + static_cast<int64_t>(nb) * ssnb] = g.s;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = vn[i];
     }
+    // after an abort, let the loads still in flight land before the CTA may exit
+    if (!ok && tid == 0) spin_ns(100000);
 }
 
 // ------------------------------------------- 1x128 -> 128x1 requantizer ----
+//
+// Persistent CTAs (two per SM) over 128 (tokens) x 128 (channels) blocks.  TMA
+// brings each 16 KB code block into an RQ_STAGES-deep ring; the block's 128
+// row scales (any strides) arrive by cp.async on the same mbarrier.  A thread
+// owns 4 adjacent channels (one 4-byte shared load per row; a warp reads a
+// whole 128-byte row) of 16 consecutive rows.  Pass 1 dequantizes (one fp32
+// multiply, xhat = decode(q) * s) into registers and takes the per-channel
+// amax; warps combine through shared memory and one thread per channel derives
+// the 128x1 scale and reciprocal.  Pass 2 quantizes the registers; per channel
+// the 16 codes of the thread's rows (16 contiguous bytes of the transposed
+// output row) go to a shared staging tile (rows skewed by a bank group every
+// 4 rows, so a warp's writes do not conflict), which is then copied out with
+// 16-byte stores, 8 lanes per 128-byte output row.  The sign of every dequantized value is the sign
+// bit of its input code, so the input bytes supply the sign bits.
+constexpr int RQ_STAGES = 4;
+constexpr int RQ_THREADS = 256;
+constexpr uint32_t RQ_TILE_BYTES = 128 * 128;
+constexpr uint32_t RQ_STAGE_OUT = 17024;   // >= stage_bytes<2>(), multiple of 128
+static_assert(RQ_STAGE_OUT >= stage_bytes<2>() && RQ_STAGE_OUT % 128 == 0, "requant staging tile");
+constexpr size_t RQ_SMEM = 128 + RQ_STAGES * RQ_TILE_BYTES + RQ_STAGE_OUT + RQ_STAGES * 128 * 4 + 8 * 128 * 4 +
+                           3 * 128 * 4 + RQ_STAGES * 8;
 
-// Eight E4M3 codes (bytes of v, in order) -> eight fp32 values decode(q) * scale,
-// one fp32 multiply each (E4M3 -> f16 -> f32 is exact).
-__device__ __forceinline__ void dequant8(const uint2 v, float scale, float2 (&xr)[4]) {
-    const uint32_t h[4] = {cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.x & 0xFFFFu)),
-                           cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.x >> 16)),
-                           cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.y & 0xFFFFu)),
-                           cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(v.y >> 16))};
-    const float2 sc = make_float2(scale, scale);
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        xr[k] = __fmul2_rn(make_float2(f16_bits_to_f32(h[k] & 0xFFFFu), f16_bits_to_f32(h[k] >> 16)), sc);
-}
+struct RequantArgs {
+    const float* s;
+    int64_t ssm, sskb;
+    uint8_t* qT;
+    int64_t ldqT;
+    float* sT;
+    int64_t sTk, sTmb;
+    int MB, KB;
+};
 
-// One CTA per 128 (rows) x 128 (channels) block per iteration.  Thread layout
-// as in the weight quantizer, on bytes: eight 8-byte loads of codes and the
-// eight row scales of its rows (the next block's are loaded before the
-// current block is processed).  Pass 1 dequantizes (one fp32 multiply) and
-// reduces the per-channel amax over the 128 rows (lane shuffle + shared
-// memory); one thread per channel derives the channel's scale and reciprocal;
-// pass 2 dequantizes again and quantizes; an 8x8 byte transpose and 8-byte
-// stores write the transposed output.  The sign of every dequantized value is
-// the sign bit of its input code, so the input bytes supply the sign bits.
-__global__ void __launch_bounds__(256, 2) k_requant_1x128_to_128x1(const uint8_t* __restrict__ q, int MB, int KB,
-                                                                   int64_t ldq, const float* __restrict__ s,
-                                                                   int64_t ssm, int64_t sskb,
-                                                                   uint8_t* __restrict__ qT, int64_t ldqT,
-                                                                   float* __restrict__ sT, int64_t sTk,
-                                                                   int64_t sTmb) {
-    __shared__ __align__(16) float red[2][8][128];
-    __shared__ __align__(16) float c_s[2][128];
-    __shared__ __align__(16) float c_r[2][128];
-    __shared__ __align__(16) int c_mode[2][128];
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int nc = lane & 15;
-    const int rb = warp * 2 + (lane >> 4);
-    const int n_blocks = MB * KB;
-    int blk = blockIdx.x;
-    if (blk >= n_blocks) return;
-    uint2 v[8];
-    float sr[8];
-    auto load = [&](int b, uint2 (&dv)[8], float (&ds)[8]) {
-        const int mb_ = b / KB;
-        const int kb_ = b - mb_ * KB;
-        const int64_t r0 = static_cast<int64_t>(mb_) * 128 + rb * 8;
-        const int64_t c0 = static_cast<int64_t>(kb_) * 128 + nc * 8;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dv[i] = ldg_nc_v2(q + (r0 + i) * ldq + c0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) ds[i] = __ldg(s + (r0 + i) * ssm + static_cast<int64_t>(kb_) * sskb);
+__global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const __grid_constant__ CUtensorMap tmQ,
+                                                                          const RequantArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    uint8_t* tiles = base;                                                        // [stage][128 m][128 k]
+    uint8_t* out = base + RQ_STAGES * RQ_TILE_BYTES;                              // staged [128 k][128 m]
+    float* sc = reinterpret_cast<float*>(out + RQ_STAGE_OUT);                    // [stage][128] row scales
+    float* red = sc + RQ_STAGES * 128;                                           // [8 warps][128 channels]
+    float* cs = red + 8 * 128;                                                   // channel scale
+    float* cr = cs + 128;                                                        // channel reciprocal
+    int* cm = reinterpret_cast<int*>(cr + 128);                                  // channel mode
+    uint64_t* full = reinterpret_cast<uint64_t*>(cm + 128);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int total = a.MB * a.KB;
+
+    // TMA of the codes (thread 0) and cp.async of the row scales (threads 0-127),
+    // both completing on full[stage]: 1 expect-tx arrival + 128 cp.async arrivals.
+    auto issue = [&](int stage, int blk) {
+        const int mb = blk / a.KB;
+        const int kb = blk - mb * a.KB;
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&full[stage], RQ_TILE_BYTES);
+            tma_load_2d(tiles + stage * RQ_TILE_BYTES, &tmQ, &full[stage], kb * 128, mb * 128);
+        }
+        if (tid < 128) {
+            cp_async_4(sc + stage * 128 + tid,
+                       a.s + static_cast<int64_t>(mb * 128 + tid) * a.ssm + static_cast<int64_t>(kb) * a.sskb);
+            cp_async_arrive_noinc(&full[stage]);
+        }
     };
-    load(blk, v, sr);
-    int par = 0;
-    for (; blk < n_blocks; blk += gridDim.x, par ^= 1) {
-        const int mb = blk / KB;
-        const int kb = blk - mb * KB;
-        const int64_t row0 = static_cast<int64_t>(mb) * 128 + rb * 8;
-        const int64_t col0 = static_cast<int64_t>(kb) * 128 + nc * 8;
-        uint2 vn[8];
-        float srn[8];
-        const int nxt = blk + gridDim.x;
-        if (nxt < n_blocks) load(nxt, vn, srn);
+    if (tid == 0) {
+        for (int i = 0; i < RQ_STAGES; ++i) mbar_init(&full[i], 129);
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+    }
+    __syncthreads();
+    for (int i = 0; i < RQ_STAGES; ++i) {
+        const int blk = blockIdx.x + i * gridDim.x;
+        if (blk < total) issue(i, blk);
+    }
 
-        // pass 1: per-channel amax of the dequantized values
-        float ca[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ca[j] = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float2 xr[4];
-            dequant8(v[i], sr[i], xr);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                ca[2 * k] = fmaxf(ca[2 * k], fabsf(xr[k].x));
-                ca[2 * k + 1] = fmaxf(ca[2 * k + 1], fabsf(xr[k].y));
-            }
+    bool ok = true;
+    for (int i = 0;; ++i) {
+        const int blk = blockIdx.x + i * gridDim.x;
+        if (blk >= total) break;
+        const int stage = i % RQ_STAGES;
+        if (!__syncthreads_and(mbar_wait(&full[stage], (i / RQ_STAGES) & 1u, nullptr))) {
+            if (tid == 0) record_status(kStatusTimeout);
+            ok = false;
+            break;
         }
+        const int mb = blk / a.KB;
+        const int kb = blk - mb * a.KB;
+        const uint8_t* tile = tiles + stage * RQ_TILE_BYTES;
+        const float* srow = sc + stage * 128 + 16 * warp;
+
+        // pass 1: dequantize 16 rows x 4 channels, per-channel amax
+        uint32_t wv[16];
+        float xv[16][4];
+        float am[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) ca[j] = fmaxf(ca[j], __shfl_xor_sync(0xffffffffu, ca[j], 16));
-        if (lane < 16) {
-            float4* dst = reinterpret_cast<float4*>(&red[par][warp][nc * 8]);
-            dst[0] = make_float4(ca[0], ca[1], ca[2], ca[3]);
-            dst[1] = make_float4(ca[4], ca[5], ca[6], ca[7]);
+        for (int rr = 0; rr < 16; ++rr) {
+            wv[rr] = lds_u32(tile + (16 * warp + rr) * 128 + 4 * lane);
+            const float sr = srow[rr];
+            const uint32_t h0 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(wv[rr] & 0xFFFFu));
+            const uint32_t h1 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(wv[rr] >> 16));
+            const float2 p0 = __fmul2_rn(make_float2(f16_bits_to_f32(h0 & 0xFFFFu), f16_bits_to_f32(h0 >> 16)),
+                                         make_float2(sr, sr));
+            const float2 p1 = __fmul2_rn(make_float2(f16_bits_to_f32(h1 & 0xFFFFu), f16_bits_to_f32(h1 >> 16)),
+                                         make_float2(sr, sr));
+            xv[rr][0] = p0.x;
+            xv[rr][1] = p0.y;
+            xv[rr][2] = p1.x;
+            xv[rr][3] = p1.y;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) am[c] = fmaxf(am[c], fabsf(xv[rr][c]));
+        }
+        *reinterpret_cast<float4*>(red + warp * 128 + 4 * lane) = make_float4(am[0], am[1], am[2], am[3]);
+        __syncthreads();
+        if (tid < 128) {   // one scale computation per channel
+            float m = red[tid];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w * 128 + tid]);
+            const GroupScale g = group_scale(m);
+            cs[tid] = g.s;
+            cr[tid] = g.r;
+            cm[tid] = g.mode;
+            a.sT[static_cast<int64_t>(kb * 128 + tid) * a.sTk + static_cast<int64_t>(mb) * a.sTmb] = g.s;
         }
         __syncthreads();
-        if (threadIdx.x < 128) {                 // one scale computation per channel
-            float a = red[par][0][threadIdx.x];
-#pragma unroll
-            for (int ww = 1; ww < 8; ++ww) a = fmaxf(a, red[par][ww][threadIdx.x]);
-            const GroupScale g = group_scale(a);
-            c_s[par][threadIdx.x] = g.s;
-            c_r[par][threadIdx.x] = g.r;
-            c_mode[par][threadIdx.x] = g.mode;
-        }
-        __syncthreads();
 
-        // pass 2: dequantize again and quantize with the channel scales
-        float cs[8], cr[8];
-        int all_recip;
-        {
-            const float4* ps = reinterpret_cast<const float4*>(&c_s[par][nc * 8]);
-            const float4* pr = reinterpret_cast<const float4*>(&c_r[par][nc * 8]);
-            const int4* pm = reinterpret_cast<const int4*>(&c_mode[par][nc * 8]);
-            const float4 s0 = ps[0], s1 = ps[1], r0 = pr[0], r1 = pr[1];
-            cs[0] = s0.x; cs[1] = s0.y; cs[2] = s0.z; cs[3] = s0.w;
-            cs[4] = s1.x; cs[5] = s1.y; cs[6] = s1.z; cs[7] = s1.w;
-            cr[0] = r0.x; cr[1] = r0.y; cr[2] = r0.z; cr[3] = r0.w;
-            cr[4] = r1.x; cr[5] = r1.y; cr[6] = r1.z; cr[7] = r1.w;
-            const int4 m0 = pm[0], m1 = pm[1];
-            // all eight channels take the reciprocal path iff the AND of their modes is 1
-            all_recip = (m0.x & m0.y & m0.z & m0.w & m1.x & m1.y & m1.z & m1.w) == 1;
-        }
-        uint2 rows[8];
-        if (all_recip) {
+        // pass 2: quantize each channel's 16 rows and write them transposed
+        const float4 s4 = *reinterpret_cast<const float4*>(cs + 4 * lane);
+        const float4 r4 = *reinterpret_cast<const float4*>(cr + 4 * lane);
+        const int4 m4 = *reinterpret_cast<const int4*>(cm + 4 * lane);
+        const float chs[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float chr[4] = {r4.x, r4.y, r4.z, r4.w};
+        const int chm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float2 xr[4];
-                dequant8(v[i], sr[i], xr);
-                uint32_t c[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    c[k] = e4m3_pair(div2_markstein(xr[k], make_float2(cr[2 * k], cr[2 * k + 1]),
-                                                    make_float2(-cs[2 * k], -cs[2 * k + 1])));
-                rows[i] = make_uint2((__byte_perm(c[0], c[1], 0x5410)) | (v[i].x & 0x80808080u),
-                                     (__byte_perm(c[2], c[3], 0x5410)) | (v[i].y & 0x80808080u));
-            }
-        } else {
-            int cm[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) cm[j] = c_mode[par][nc * 8 + j];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                float2 xr[4];
-                dequant8(v[i], sr[i], xr);
-                uint32_t cw[2] = {0u, 0u};
+        for (int c = 0; c < 4; ++c) {
+            uint32_t o4[4];
+            if (chm[c] == 1) {
+                const float2 r2 = make_float2(chr[c], chr[c]);
+                const float2 ns2 = make_float2(-chs[c], -chs[c]);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const uint32_t c = quant_div(xr[k].x, cs[2 * k], cm[2 * k]) |
-                                       (quant_div(xr[k].y, cs[2 * k + 1], cm[2 * k + 1]) << 8);
-                    cw[k >> 1] |= c << (16 * (k & 1));
+                    const uint32_t c0 =
+                        e4m3_pair(div2_markstein(make_float2(xv[4 * k][c], xv[4 * k + 1][c]), r2, ns2));
+                    const uint32_t c1 =
+                        e4m3_pair(div2_markstein(make_float2(xv[4 * k + 2][c], xv[4 * k + 3][c]), r2, ns2));
+                    // byte c of the four input words: their sign bits are the codes' sign bits
+                    const uint32_t sel = static_cast<uint32_t>(c) | (static_cast<uint32_t>(c + 4) << 4);
+                    const uint32_t in4 = __byte_perm(__byte_perm(wv[4 * k], wv[4 * k + 1], sel),
+                                                     __byte_perm(wv[4 * k + 2], wv[4 * k + 3], sel), 0x5410);
+                    o4[k] = __byte_perm(c0, c1, 0x5410) | (in4 & 0x80808080u);
                 }
-                rows[i] = make_uint2(cw[0], cw[1]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t o = 0u;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) o |= quant_div(xv[4 * k + u][c], chs[c], chm[c]) << (8 * u);
+                    o4[k] = o;
+                }
             }
+            sts_v4(out + stage_row<2>(4 * lane + c) + 16 * warp, make_uint4(o4[0], o4[1], o4[2], o4[3]));
         }
-        uint2 cols[8];
-        transpose8x8(rows, cols);
+        __syncthreads();   // staged tile complete; this stage, red[] and the channel scales are free
+        uint8_t* dst = a.qT + static_cast<int64_t>(kb * 128) * a.ldqT + mb * 128;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) stg_v2(qT + (col0 + j) * ldqT + row0, cols[j]);
-        if (rb == 0) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) sT[(col0 + j) * sTk + static_cast<int64_t>(mb) * sTmb] = cs[j];
+        for (int u = 0; u < 4; ++u) {
+            const int id = tid + RQ_THREADS * u;    // 128 rows x 8 chunks of 16 bytes
+            const int row = id >> 3, ch = id & 7;
+            stg_v4(dst + static_cast<int64_t>(row) * a.ldqT + 16 * ch, lds_v4(out + stage_row<2>(row) + 16 * ch));
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[i] = vn[i];
-            sr[i] = srn[i];
-        }
+        const int nxt = blk + RQ_STAGES * gridDim.x;
+        if (nxt < total) issue(stage, nxt);
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!ok && tid == 0) spin_ns(100000);
 }
 
 }  // namespace fp8fg

@@ -2,8 +2,8 @@
 
     python -m fp8_fine_grained_20_b300.profile_case KERNEL [--launches N] [--warmup W]
 
-KERNEL is one of quant_act, quant_w, requant, gemm_fprop, gemm_wgrad,
-grouped_gemm.  The process allocates only what that one call needs (at most
+KERNEL is one of quant_act, quant_w, quant_w_moe (32 experts in one batched
+launch), requant, gemm_fprop, gemm_wgrad, grouped_gemm.  The process allocates only what that one call needs (at most
 about 2 GB), fills the bf16 inputs on the device with torch's generator
 (N(0,1) activations with 1% of channels x100, N(0, 0.02^2) weights,
 N(0, 1e-3^2) gradients), quantizes them with the library where the kernel
@@ -33,11 +33,13 @@ def _gen(seed):
 
 def activation(rows, cols, seed):
     g = _gen(seed)
-    x = torch.randn((rows, cols), generator=g, device="cuda", dtype=torch.float32)
-    n_out = round(0.01 * cols)
-    idx = torch.randperm(cols, generator=g, device="cuda")[:n_out]
-    x[:, idx] *= 100.0
-    return x.to(torch.bfloat16)
+    idx = torch.randperm(cols, generator=g, device="cuda")[:round(0.01 * cols)]
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, rows, 8192):       # fp32 temporaries of at most 8192 rows
+        x = torch.randn((min(8192, rows - r0), cols), generator=g, device="cuda", dtype=torch.float32)
+        x[:, idx] *= 100.0
+        out[r0:r0 + x.shape[0]] = x.to(torch.bfloat16)
+    return out
 
 
 def weight(rows, cols, seed, sigma=0.02):
@@ -70,6 +72,11 @@ def setup(kind):
         q = torch.empty((COUT, CIN), dtype=torch.uint8, device="cuda")
         s = torch.empty((CIN // 128, COUT // 128), dtype=torch.float32, device="cuda")
         return lambda: fg.fp8_quant_w_128x128(w, q, s)
+    if kind == "quant_w_moe":
+        w = weight(G * MOE_K, MOE_N, 10).view(G, MOE_K, MOE_N)
+        q = torch.empty((G, MOE_N, MOE_K), dtype=torch.uint8, device="cuda")
+        s = torch.empty((G, MOE_K // 128, MOE_N // 128), dtype=torch.float32, device="cuda")
+        return lambda: fg.fp8_quant_w_128x128_batched(w, q, s)
     if kind == "requant":
         q, s = fg.fp8_quant_act_1x128(activation(T, CIN, 3))
         qT = torch.empty((CIN, T), dtype=torch.uint8, device="cuda")
@@ -92,10 +99,7 @@ def setup(kind):
         off = moe_offsets(8)
         rows = int(off[-1])
         a, sa = fg.fp8_quant_act_1x128(activation(rows, MOE_K, 9))
-        bq = torch.empty((G, MOE_N, MOE_K), dtype=torch.uint8, device="cuda")
-        bs = torch.empty((G, MOE_K // 128, MOE_N // 128), dtype=torch.float32, device="cuda")
-        for e in range(G):
-            fg.fp8_quant_w_128x128(weight(MOE_K, MOE_N, 100 + e), bq[e], bs[e])
+        bq, bs = fg.fp8_quant_w_128x128_batched(weight(G * MOE_K, MOE_N, 100).view(G, MOE_K, MOE_N))
         c = torch.empty((rows, MOE_N), dtype=torch.bfloat16, device="cuda")
         d_off = off.cuda()
         return lambda: fg.fp8_grouped_gemm_blockscaled(a, sa, bq, bs, d_off, c)
@@ -104,8 +108,8 @@ def setup(kind):
 
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    p.add_argument("kernel", choices=["quant_act", "quant_w", "requant", "gemm_fprop", "gemm_wgrad",
-                                      "grouped_gemm"])
+    p.add_argument("kernel", choices=["quant_act", "quant_w", "quant_w_moe", "requant", "gemm_fprop",
+                                      "gemm_wgrad", "grouped_gemm"])
     p.add_argument("--launches", type=int, default=1)
     p.add_argument("--warmup", type=int, default=2)
     args = p.parse_args(argv)
@@ -113,6 +117,7 @@ def main(argv=None):
     fg.capi()
     run = setup(args.kernel)
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()    # release the generators' fp32 temporaries before any capture
     for _ in range(args.warmup + args.launches):
         run()
     torch.cuda.synchronize()

@@ -107,6 +107,22 @@ fp8_status_t fp8_quant_w_128x128(const uint16_t* w, int64_t K, int64_t N, int64_
                                  void* stream);
 
 /*
+ * 128x128 quantization of a batch of G weights in one launch (the experts of
+ * an MoE layer; sunipension.com post 314414, Figure 7(a), applied per expert).
+ * Weight g is w + g * w_batch_stride, its codes q + g * q_batch_stride and its
+ * scales s + g * s_batch_stride; everything else is as in fp8_quant_w_128x128,
+ * which is this call with G = 1.  For G > 1 the batch strides (elements) must
+ * not make weights or code blocks overlap, and w_batch_stride * 2 and
+ * q_batch_stride must be multiples of 16 bytes.
+ */
+fp8_status_t fp8_quant_w_128x128_batched(const uint16_t* w, int64_t G, int64_t K, int64_t N, int64_t ldw,
+                                         int64_t w_batch_stride,
+                                         uint8_t* q, int64_t ldq, int64_t q_batch_stride, int q_layout,
+                                         float* s, int64_t s_stride_kb, int64_t s_stride_nb,
+                                         int64_t s_batch_stride,
+                                         void* stream);
+
+/*
  * 1x128 -> 128x1 requantization for the backward pass (sunipension.com post
  * 314414: cached 1x128 activation tiles become 128x1 tiles).  Every value is
  * dequantized with one fp32 multiply, xhat = decode(q) * s, then every

@@ -219,6 +219,60 @@ def test_weight_full_quantizer_workload(orc):
     check_w(orc, synth.weight(2, 7168, 18432))
 
 
+def test_weight_padded_rows(orc):
+    """Row strides larger than the row (ldw = N + 64, ldq padded) in both layouts."""
+    K, N = 256, 384
+    bits = synth.weight(22, K, N)
+    q_ref, s_ref = orc.quant_w_128x128(bits)
+    wpad = np.zeros((K, N + 64), np.uint16)
+    wpad[:, :N] = bits
+    w = gu.bf16_dev(wpad)[:, :N]
+    qk = torch.full((N, K + 32), 0xAB, dtype=torch.uint8, device="cuda")
+    q, s = fg.fp8_quant_w_128x128(w, q=qk[:, :K])
+    torch.cuda.synchronize()
+    assert_bits_eq(gu.host(q), q_ref.T, "weight codes (K-major, padded)")
+    assert_bits_eq(gu.host(s), s_ref, "weight scales (padded)")
+    assert np.all(gu.host(qk)[:, K:] == 0xAB), "write outside the code rows"
+    qr = torch.full((K, N + 16), 0xAB, dtype=torch.uint8, device="cuda")
+    q2, _ = fg.fp8_quant_w_128x128(w, q=qr[:, :N], q_layout=fg.FP8_ROWMAJOR_KN)
+    torch.cuda.synchronize()
+    assert_bits_eq(gu.host(q2), q_ref, "weight codes (row-major, padded)")
+    assert np.all(gu.host(qr)[:, N:] == 0xAB), "write outside the code rows"
+
+
+@pytest.mark.parametrize("q_layout", [0, 1])
+def test_weight_batched_matches_oracle_per_expert(orc, q_layout):
+    """One launch over G experts with a padded expert stride; every expert's
+    codes and scales equal the oracle's for that expert alone."""
+    G, K, N = 3, 256, 384
+    experts = [synth.weight(30 + g, K, N) for g in range(G)]
+    experts[1] = np.zeros((K, N), np.uint16)          # an all-zero expert
+    wbuf = np.zeros((G, K + 128, N), np.uint16)
+    for g in range(G):
+        wbuf[g, :K] = experts[g]
+    w = gu.bf16_dev(wbuf)[:, :K, :]
+    q, s = fg.fp8_quant_w_128x128_batched(w, q_layout=q_layout)
+    torch.cuda.synchronize()
+    q, s = gu.host(q), gu.host(s)
+    for g in range(G):
+        q_ref, s_ref = orc.quant_w_128x128(experts[g])
+        assert_bits_eq(s[g], s_ref, "expert %d scales" % g)
+        assert_bits_eq(q[g], q_ref.T if q_layout == 0 else q_ref, "expert %d codes" % g)
+
+
+def test_weight_batched_moe_experts(orc):
+    """The MoE expert weights of the benchmark step (32 x [7168, 2048]), spot-
+    checked on four experts."""
+    moe = synth.moe_inputs(seed=5, with_weights=True)
+    w = gu.bf16_dev(moe.w)
+    q, s = fg.fp8_quant_w_128x128_batched(w)
+    torch.cuda.synchronize()
+    for g in (0, 7, 19, 31):
+        q_ref, s_ref = orc.quant_w_128x128(moe.w[g])
+        assert_bits_eq(gu.host(s[g]), s_ref, "expert %d scales" % g)
+        assert_bits_eq(gu.host(q[g]), q_ref.T, "expert %d codes" % g)
+
+
 # ---------------------------------------------------------------- requant --
 
 def run_requant(q_np, s_np, s_layout_in="mn"):
@@ -258,6 +312,23 @@ def test_requant_edge_scales(orc):
     qT, sT = run_requant(q, s)
     assert_bits_eq(sT, sT_ref, "requant scales")
     assert_bits_eq(qT, qT_ref, "requant codes")
+
+
+def test_requant_padded_strides(orc):
+    """ldq > K, ldqT > M and row-major input scales."""
+    bits = synth.wgrad_tensor(4, 1, 256, 384)
+    q, s = orc.quant_act_1x128(bits)
+    qT_ref, sT_ref = orc.requant_1x128_to_128x1(q, s)
+    M, K = q.shape
+    qpad = np.zeros((M, K + 48), np.uint8)
+    qpad[:, :K] = q
+    qd = gu.dev(qpad)[:, :K]
+    qTbuf = torch.full((K, M + 16), 0xAB, dtype=torch.uint8, device="cuda")
+    qT, sT = fg.fp8_requant_1x128_to_128x1(qd, gu.dev(s), qT=qTbuf[:, :M], scale_layout="row")
+    torch.cuda.synchronize()
+    assert_bits_eq(gu.host(sT), sT_ref, "requant scales")
+    assert_bits_eq(gu.host(qT), qT_ref, "requant codes")
+    assert np.all(gu.host(qTbuf)[:, M:] == 0xAB), "write outside the code rows"
 
 
 def test_requant_full_quantizer_workload(orc):
