@@ -7,7 +7,10 @@ FP8 training step of a large MoE transformer layer:
   forward of an FP8 linear layer      X bf16 [8192, 7168] -> 1x128 quantize;
                                       W bf16 [7168, 18432] -> 128x128 quantize;
                                       Y = GEMM (1x128 x 128x128 scales) bf16 [8192, 18432]
-  weight gradient of that layer       dY bf16 [8192, 18432] -> 1x128 quantize;
+  data gradient of that layer         dY bf16 [8192, 18432] -> 1x128 quantize;
+                                      W -> 128x128 quantize (row-major codes);
+                                      dX = GEMM (1x128 x 128x128 scales) bf16 [8192, 7168]
+  weight gradient of that layer       (dY quantized above)
                                       cached Xq and dYq -> 1x128 -> 128x1 requantize;
                                       dW = GEMM (128x1 x 128x1 scales) bf16 [7168, 18432]
   MoE expert forward                  16384 tokens x 8 picks (Zipf 1.1 over 32 experts,
@@ -15,7 +18,7 @@ FP8 training step of a large MoE transformer layer:
                                       32 experts W_g [7168, 2048] -> 128x128 quantize;
                                       grouped GEMM -> bf16 [~133k, 2048]
 
-`value` is the step's GEMM work (2MNK summed over the three GEMMs, routed rows
+`value` is the step's GEMM work (2MNK summed over the four GEMMs, routed rows
 for the MoE) divided by the step time, summed over ranks: whole-step TFLOP/s,
 quantizers included.  Inputs live in HBM before the timed region; every input
 is larger than L2 or is followed by larger traffic.  `e2e` repeats the step
@@ -88,6 +91,7 @@ class Workload:
     def gemm_flops(self):
         return {
             "gemm_fprop": 2.0 * T * COUT * CIN,
+            "gemm_dgrad": 2.0 * T * CIN * COUT,
             "gemm_wgrad": 2.0 * CIN * COUT * T,
             "grouped_gemm_moe": 2.0 * self.routed_rows * MOE_N * MOE_K,
         }
@@ -101,6 +105,7 @@ class Workload:
         return {
             "quant_act_x": q(T, CIN),
             "quant_w": q(CIN, COUT) - CIN * COUT // 128 * 4 + (CIN // 128) * (COUT // 128) * 4,
+            "quant_w_rowmajor": q(CIN, COUT) - CIN * COUT // 128 * 4 + (CIN // 128) * (COUT // 128) * 4,
             "quant_act_dy": q(T, COUT),
             "requant_x": rq(T, CIN),
             "requant_dy": rq(T, COUT),
@@ -111,14 +116,17 @@ class Workload:
     def describe(self):
         return {
             "workload": "FP8 training step of one MoE transformer layer: linear fwd "
-                        "[8192x7168]x[7168x18432] + wgrad (dW [7168x18432], K=8192 tokens) + "
+                        "[8192x7168]x[7168x18432] + dgrad (dX [8192x7168], K=18432) + "
+                        "wgrad (dW [7168x18432], K=8192 tokens) + "
                         "MoE grouped fwd (32 experts [7168x2048], 16384 tokens x 8, Zipf 1.1)",
             "fprop": {"M": T, "N": COUT, "K": CIN},
+            "dgrad": {"M": T, "N": CIN, "K": COUT},
             "wgrad": {"M": CIN, "N": COUT, "K": T},
             "moe": {"experts": G, "N": MOE_N, "K": MOE_K, "routed_rows": self.routed_rows,
                     "padded_rows": self.moe_rows},
             "quantizers": "1x128 act [8192x7168], [8192x18432], [%dx7168]; 128x128 weight "
-                          "[7168x18432], 32x[7168x2048]; 1x128->128x1 requant of [8192x7168], "
+                          "[7168x18432] (K-major and row-major codes), 32x[7168x2048]; "
+                          "1x128->128x1 requant of [8192x7168], "
                           "[8192x18432]" % self.moe_rows,
             "l2": "inputs larger than L2 (126 MB); %.1f GB of quantizer traffic per step"
                   % (sum(self.quant_bytes().values()) / 1e9),
@@ -132,9 +140,9 @@ class Workload:
 class DeviceStep:
     """Device buffers and the sequence of library calls of one step."""
 
-    KERNELS = ["quant_act_x", "quant_w", "gemm_fprop", "quant_act_dy", "requant_x", "requant_dy",
-               "gemm_wgrad", "quant_act_moe", "quant_w_moe", "grouped_gemm_moe"]
-    LAUNCHES_PER_STEP = 10      # the 32 expert weights are quantized in one batched launch
+    KERNELS = ["quant_act_x", "quant_w", "gemm_fprop", "quant_act_dy", "quant_w_rowmajor", "gemm_dgrad",
+               "requant_x", "requant_dy", "gemm_wgrad", "quant_act_moe", "quant_w_moe", "grouped_gemm_moe"]
+    LAUNCHES_PER_STEP = 12      # the 32 expert weights are quantized in one batched launch
 
     def __init__(self, wl, device):
         import torch
@@ -157,6 +165,7 @@ class DeviceStep:
         # intermediates (scales MN-major: logical [rows, groups] views with stride 1 along rows)
         self.xq, self.sx = e((T, CIN), u8), e((CIN // 128, T), f32).t()
         self.wq, self.sw = e((COUT, CIN), u8), e((CIN // 128, COUT // 128), f32)
+        self.wq_rm, self.sw_rm = e((CIN, COUT), u8), e((CIN // 128, COUT // 128), f32)
         self.dyq, self.sdy = e((T, COUT), u8), e((COUT // 128, T), f32).t()
         self.xqT, self.sxT = e((CIN, T), u8), e((T // 128, CIN), f32).t()
         self.dyqT, self.sdyT = e((COUT, T), u8), e((T // 128, COUT), f32).t()
@@ -164,6 +173,7 @@ class DeviceStep:
         self.mwq, self.smw = e((G, MOE_N, MOE_K), u8), e((G, MOE_K // 128, MOE_N // 128), f32)
         # outputs
         self.y = e((T, COUT), bf)
+        self.dx = e((T, CIN), bf)
         self.dw = e((CIN, COUT), bf)
         self.moe_y = e((wl.moe_rows, MOE_N), bf)
         self.load_inputs(wl)
@@ -203,6 +213,13 @@ class DeviceStep:
         rec("quant_act_dy", 0)
         fg.fp8_quant_act_1x128(self.dy, self.dyq, self.sdy, stream=stream)
         rec("quant_act_dy", 1)
+        rec("quant_w_rowmajor", 0)
+        fg.fp8_quant_w_128x128(self.w, self.wq_rm, self.sw_rm, q_layout=fg.FP8_ROWMAJOR_KN, stream=stream)
+        rec("quant_w_rowmajor", 1)
+        rec("gemm_dgrad", 0)
+        fg.fp8_gemm_blockscaled(self.dyq, self.sdy, self.wq_rm, self.sw_rm.t(), fg.FP8_SB_BLOCK128x128, self.dx,
+                                stream=stream)
+        rec("gemm_dgrad", 1)
         rec("requant_x", 0)
         fg.fp8_requant_1x128_to_128x1(self.xq, self.sx, self.xqT, self.sxT, stream=stream)
         rec("requant_x", 1)
@@ -349,7 +366,8 @@ def cpu_oracle_sample(wl, frac, threads=1):
         est += dt * n_full / (rows * arr.shape[1])
         parts.append("act %s %d rows" % (name, rows))
     # 128x128 weight quantization: one 128-row block strip, a fraction of its columns
-    for name, arr, n_full in (("w", wl.w, CIN * COUT), ("moe_w", wl.moe_w[0], G * MOE_K * MOE_N)):
+    for name, arr, n_full in (("w", wl.w, CIN * COUT), ("w_rowmajor", wl.w, CIN * COUT),
+                              ("moe_w", wl.moe_w[0], G * MOE_K * MOE_N)):
         cols = max(128, int(round(frac * arr.size / 128)) // 128 * 128)
         cols = min(cols, arr.shape[1])
         _, dt = timed(lambda: oracle.quant_w_128x128(np.ascontiguousarray(arr[:128, :cols]), threads=threads))
@@ -370,19 +388,21 @@ def cpu_oracle_sample(wl, frac, threads=1):
     xq, xs = oracle.quant_act_1x128(wl.x[:128])
     wq, ws = oracle.quant_w_128x128(np.ascontiguousarray(wl.w[:, :128]))
     wt = np.ascontiguousarray(wq.T)
-    for name, n_out in (("fprop", T * COUT), ("wgrad", CIN * COUT), ("moe", wl.routed_rows * MOE_N)):
-        k = T if name == "wgrad" else CIN
+    depth = {"fprop": CIN, "dgrad": COUT, "wgrad": T, "moe": MOE_K}
+    for name, n_out in (("fprop", T * COUT), ("dgrad", T * CIN), ("wgrad", CIN * COUT),
+                        ("moe", wl.routed_rows * MOE_N)):
+        k = depth[name]
         cnt = max(16, int(round(frac * n_out)))
         ms = rng.integers(0, 128, cnt)
         ns = rng.integers(0, 128, cnt)
         if k == CIN:
             a, sa, b, sb = xq, xs, wt, ws
-        else:  # K = 8192 tokens: tile the 7168-deep strips up to the token count
-            reps = -(-T // CIN)
-            a = np.tile(xq, (1, reps))[:, :T]
-            sa = np.tile(xs, (1, reps))[:, :T // 128]
-            b = np.tile(wt, (1, reps))[:, :T]
-            sb = np.tile(ws, (reps, 1))[:T // 128]
+        else:  # a deeper reduction: tile the 7168-deep strips up to K
+            reps = -(-k // CIN)
+            a = np.tile(xq, (1, reps))[:, :k]
+            sa = np.tile(xs, (1, reps))[:, :k // 128]
+            b = np.tile(wt, (1, reps))[:, :k]
+            sb = np.tile(ws, (reps, 1))[:k // 128]
         _, dt = timed(lambda: oracle.gemm_blockscaled_sample(a, sa, b, sb, oracle.SB_BLOCK128x128, ms, ns,
                                                              threads=threads))
         t_total += dt
@@ -582,6 +602,7 @@ def run_e2e(args, wl, step, stream, total_flops, world, device):
             (pinned(wl.moe_w.view(np.int16), torch.bfloat16), step.moe_w),
             (pinned(wl.moe_offsets), step.moe_off)]
     h_out = [(step.y, torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()),
+             (step.dx, torch.empty(step.dx.shape, dtype=step.dx.dtype).pin_memory()),
              (step.dw, torch.empty(step.dw.shape, dtype=step.dw.dtype).pin_memory()),
              (step.moe_y, torch.empty(step.moe_y.shape, dtype=step.moe_y.dtype).pin_memory())]
     h2d = sum(h.numel() * h.element_size() for h, _ in h_in)

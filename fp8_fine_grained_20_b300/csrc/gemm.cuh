@@ -19,7 +19,7 @@
 //     A from each CTA's own shared memory and half of B's 256 rows from each
 //     CTA, so every SM loads 32 KB per 128-deep K-block instead of 48 KB;
 //   * warp 0 (both CTAs): TMA producer -- this CTA's A box (128 x 128 B) and B
-//     half (128 x 128 B), 128-byte swizzle, 6-stage ring; the transaction
+//     half (128 x 128 B), 128-byte swizzle, 5-stage ring; the transaction
 //     bytes of both CTAs are counted on the even CTA's "full" barrier;
 //   * warp 1 (even CTA): MMA issuer -- per K-block, 4 x tcgen05.mma (K = 32)
 //     into one of two 256-column TMEM partial buffers, then one commit to the
@@ -47,7 +47,7 @@ constexpr int PM = 256;           // rows per CTA pair (MMA M)
 constexpr int BN = 256;           // columns per tile (MMA N)
 constexpr int BNH = BN / 2;       // B rows loaded by each CTA
 constexpr int BK = 128;
-constexpr int STAGES = 6;
+constexpr int STAGES = 5;
 constexpr int SSLOTS = 8;
 constexpr int THREADS = 384;
 constexpr int PROMO_WARPS = 8;

@@ -396,10 +396,12 @@ __global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_
 // bit of its input code, so the input bytes supply the sign bits.
 constexpr int RQ_STAGES = 4;
 constexpr int RQ_THREADS = 256;
+constexpr int RQ_WARPS = RQ_THREADS / 32;
+constexpr int RQ_ROWS = 128 / RQ_WARPS;    // rows per thread
 constexpr uint32_t RQ_TILE_BYTES = 128 * 128;
 constexpr uint32_t RQ_STAGE_OUT = 17024;   // >= stage_bytes<2>(), multiple of 128
 static_assert(RQ_STAGE_OUT >= stage_bytes<2>() && RQ_STAGE_OUT % 128 == 0, "requant staging tile");
-constexpr size_t RQ_SMEM = 128 + RQ_STAGES * RQ_TILE_BYTES + RQ_STAGE_OUT + RQ_STAGES * 128 * 4 + 8 * 128 * 4 +
+constexpr size_t RQ_SMEM = 128 + RQ_STAGES * RQ_TILE_BYTES + RQ_STAGE_OUT + RQ_STAGES * 128 * 4 + RQ_WARPS * 128 * 4 +
                            3 * 128 * 4 + RQ_STAGES * 8;
 
 struct RequantArgs {
@@ -419,8 +421,8 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
     uint8_t* tiles = base;                                                        // [stage][128 m][128 k]
     uint8_t* out = base + RQ_STAGES * RQ_TILE_BYTES;                              // staged [128 k][128 m]
     float* sc = reinterpret_cast<float*>(out + RQ_STAGE_OUT);                    // [stage][128] row scales
-    float* red = sc + RQ_STAGES * 128;                                           // [8 warps][128 channels]
-    float* cs = red + 8 * 128;                                                   // channel scale
+    float* red = sc + RQ_STAGES * 128;                                           // [warp][128 channels]
+    float* cs = red + RQ_WARPS * 128;                                                   // channel scale
     float* cr = cs + 128;                                                        // channel reciprocal
     int* cm = reinterpret_cast<int*>(cr + 128);                                  // channel mode
     uint64_t* full = reinterpret_cast<uint64_t*>(cm + 128);
@@ -468,15 +470,15 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
         const int mb = blk / a.KB;
         const int kb = blk - mb * a.KB;
         const uint8_t* tile = tiles + stage * RQ_TILE_BYTES;
-        const float* srow = sc + stage * 128 + 16 * warp;
+        const float* srow = sc + stage * 128 + RQ_ROWS * warp;
 
         // pass 1: dequantize 16 rows x 4 channels, per-channel amax
-        uint32_t wv[16];
-        float xv[16][4];
+        uint32_t wv[RQ_ROWS];
+        float xv[RQ_ROWS][4];
         float am[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-            wv[rr] = lds_u32(tile + (16 * warp + rr) * 128 + 4 * lane);
+        for (int rr = 0; rr < RQ_ROWS; ++rr) {
+            wv[rr] = lds_u32(tile + (RQ_ROWS * warp + rr) * 128 + 4 * lane);
             const float sr = srow[rr];
             const uint32_t h0 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(wv[rr] & 0xFFFFu));
             const uint32_t h1 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(wv[rr] >> 16));
@@ -496,7 +498,7 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
         if (tid < 128) {   // one scale computation per channel
             float m = red[tid];
 #pragma unroll
-            for (int w = 1; w < 8; ++w) m = fmaxf(m, red[w * 128 + tid]);
+            for (int w = 1; w < RQ_WARPS; ++w) m = fmaxf(m, red[w * 128 + tid]);
             const GroupScale g = group_scale(m);
             cs[tid] = g.s;
             cr[tid] = g.r;
@@ -514,12 +516,12 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
         const int chm[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            uint32_t o4[4];
+            uint32_t o4[RQ_ROWS / 4];
             if (chm[c] == 1) {
                 const float2 r2 = make_float2(chr[c], chr[c]);
                 const float2 ns2 = make_float2(-chs[c], -chs[c]);
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < RQ_ROWS / 4; ++k) {
                     const uint32_t c0 =
                         e4m3_pair(div2_markstein(make_float2(xv[4 * k][c], xv[4 * k + 1][c]), r2, ns2));
                     const uint32_t c1 =
@@ -532,19 +534,19 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < RQ_ROWS / 4; ++k) {
                     uint32_t o = 0u;
 #pragma unroll
                     for (int u = 0; u < 4; ++u) o |= quant_div(xv[4 * k + u][c], chs[c], chm[c]) << (8 * u);
                     o4[k] = o;
                 }
             }
-            sts_v4(out + stage_row<2>(4 * lane + c) + 16 * warp, make_uint4(o4[0], o4[1], o4[2], o4[3]));
+            sts_v4(out + stage_row<2>(4 * lane + c) + RQ_ROWS * warp, make_uint4(o4[0], o4[1], o4[2], o4[3]));
         }
         __syncthreads();   // staged tile complete; this stage, red[] and the channel scales are free
         uint8_t* dst = a.qT + static_cast<int64_t>(kb * 128) * a.ldqT + mb * 128;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 1024 / RQ_THREADS; ++u) {
             const int id = tid + RQ_THREADS * u;    // 128 rows x 8 chunks of 16 bytes
             const int row = id >> 3, ch = id & 7;
             stg_v4(dst + static_cast<int64_t>(row) * a.ldqT + 16 * ch, lds_v4(out + stage_row<2>(row) + 16 * ch));

@@ -3,7 +3,7 @@
     python -m fp8_fine_grained_20_b300.profile_case KERNEL [--launches N] [--warmup W]
 
 KERNEL is one of quant_act, quant_w, quant_w_moe (32 experts in one batched
-launch), requant, gemm_fprop, gemm_wgrad, grouped_gemm.  The process allocates only what that one call needs (at most
+launch), requant, gemm_fprop, gemm_dgrad, gemm_wgrad, grouped_gemm.  The process allocates only what that one call needs (at most
 about 2 GB), fills the bf16 inputs on the device with torch's generator
 (N(0,1) activations with 1% of channels x100, N(0, 0.02^2) weights,
 N(0, 1e-3^2) gradients), quantizes them with the library where the kernel
@@ -15,11 +15,16 @@ Kernel names to filter on: k_quant_act_1x128, k_quant_w_128x128,
 k_requant_1x128_to_128x1, k_gemm_blockscaled.
 """
 import argparse
+import os
 import sys
 
 import torch
 
 import fp8_fine_grained_20_b300 as fg
+
+_ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
 
 T, CIN, COUT = 8192, 7168, 18432
 G, MOE_K, MOE_N, TOKENS, TOPK, ZIPF = 32, 7168, 2048, 16384, 8, 1.1
@@ -48,16 +53,11 @@ def weight(rows, cols, seed, sigma=0.02):
 
 
 def moe_offsets(seed):
-    """Padded per-expert row ranges: Multinomial(16384 x 8, p_g ~ (g+1)^-1.1)."""
-    g = torch.Generator()
-    g.manual_seed(seed)
-    p = torch.arange(1, G + 1, dtype=torch.float64) ** (-ZIPF)
-    picks = torch.multinomial(p / p.sum(), TOKENS * TOPK, replacement=True, generator=g)
-    counts = torch.bincount(picks, minlength=G)
-    padded = (counts + 127) // 128 * 128
-    off = torch.zeros(G + 1, dtype=torch.int64)
-    off[1:] = torch.cumsum(padded, 0)
-    return off.to(torch.int32)
+    """Padded per-expert row ranges of the benchmark's MoE workload (the seeded
+    routing of the `synth` input module: 16384 tokens x 8 picks, p_g ~ (g+1)^-1.1)."""
+    import synth
+    _, offsets = synth.moe_routing(seed, G, TOKENS, TOPK, ZIPF)
+    return torch.from_numpy(offsets)
 
 
 def setup(kind):
@@ -87,6 +87,11 @@ def setup(kind):
         b, sb = fg.fp8_quant_w_128x128(weight(CIN, COUT, 5))
         c = torch.empty((T, COUT), dtype=torch.bfloat16, device="cuda")
         return lambda: fg.fp8_gemm_blockscaled(a, sa, b, sb, fg.FP8_SB_BLOCK128x128, c)
+    if kind == "gemm_dgrad":
+        a, sa = fg.fp8_quant_act_1x128(weight(T, COUT, 11, 1e-3))
+        b, sb = fg.fp8_quant_w_128x128(weight(CIN, COUT, 12), q_layout=fg.FP8_ROWMAJOR_KN)
+        c = torch.empty((T, CIN), dtype=torch.bfloat16, device="cuda")
+        return lambda: fg.fp8_gemm_blockscaled(a, sa, b, sb.t(), fg.FP8_SB_BLOCK128x128, c)
     if kind == "gemm_wgrad":
         xq, xs = fg.fp8_quant_act_1x128(weight(T, CIN, 6, 1e-3))
         dq, ds = fg.fp8_quant_act_1x128(weight(T, COUT, 7, 1e-3))
@@ -96,7 +101,7 @@ def setup(kind):
         c = torch.empty((CIN, COUT), dtype=torch.bfloat16, device="cuda")
         return lambda: fg.fp8_gemm_blockscaled(a, sa, b, sb.t(), fg.FP8_SB_COL128x1, c)
     if kind == "grouped_gemm":
-        off = moe_offsets(8)
+        off = moe_offsets(5)
         rows = int(off[-1])
         a, sa = fg.fp8_quant_act_1x128(activation(rows, MOE_K, 9))
         bq, bs = fg.fp8_quant_w_128x128_batched(weight(G * MOE_K, MOE_N, 100).view(G, MOE_K, MOE_N))
@@ -109,7 +114,7 @@ def setup(kind):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("kernel", choices=["quant_act", "quant_w", "quant_w_moe", "requant", "gemm_fprop",
-                                      "gemm_wgrad", "grouped_gemm"])
+                                      "gemm_dgrad", "gemm_wgrad", "grouped_gemm"])
     p.add_argument("--launches", type=int, default=1)
     p.add_argument("--warmup", type=int, default=2)
     args = p.parse_args(argv)

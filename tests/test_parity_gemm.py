@@ -136,6 +136,42 @@ def test_gemm_block_scales_strided(orc):
     assert torch.equal(C1, C2)
 
 
+def dgrad_operands(orc, T, Cin, Cout, seed, threads=None):
+    """dX[T, Cin] = dY W^T: dY 1x128-quantized along Cout (the reduction), W
+    128x128-quantized in its forward layout [Cin, Cout], which is already the
+    K-major B operand of this GEMM; the 128x128 scale grid is read transposed."""
+    dy = synth.wgrad_tensor(seed, 1, T, Cout)
+    w = synth.weight(seed, Cin, Cout)
+    qdy, sdy = orc.quant_act_1x128(dy, threads=threads)
+    qw, sw = orc.quant_w_128x128(w, threads=threads)          # [Cin, Cout], [Cin/128, Cout/128]
+    return qdy, sdy, qw, sw
+
+
+@pytest.mark.parametrize("T,Cin,Cout", [(256, 384, 512), (128, 128, 128), (384, 256, 1024)])
+def test_gemm_dgrad_shapes(orc, T, Cin, Cout):
+    qa, sa, qw, sw = dgrad_operands(orc, T, Cin, Cout, seed=T + Cout)
+    ref = orc.gemm_blockscaled(qa, sa, qw, np.ascontiguousarray(sw.T), orc.SB_BLOCK128x128)
+    C = fg.fp8_gemm_blockscaled(gu.dev(qa), scales_dev(sa, "mn"), gu.dev(qw), gu.dev(sw).t(),
+                                fg.FP8_SB_BLOCK128x128)
+    torch.cuda.synchronize()
+    gu.assert_gemm_close(gu.host_bf16_as_f64(C), ref, "dgrad %dx%dx%d" % (T, Cin, Cout))
+
+
+def test_dgrad_end_to_end_with_gpu_quantizers(orc):
+    """The backward-data path as a user runs it: dY 1x128 and W 128x128 (row-major
+    codes) quantized on the GPU, then the GEMM; against the oracle's chain."""
+    T, Cin, Cout = 256, 384, 640
+    dy = synth.wgrad_tensor(41, 1, T, Cout)
+    w = synth.weight(41, Cin, Cout)
+    qdy, sdy = fg.fp8_quant_act_1x128(gu.bf16_dev(dy))
+    qw, sw = fg.fp8_quant_w_128x128(gu.bf16_dev(w), q_layout=fg.FP8_ROWMAJOR_KN)
+    C = fg.fp8_gemm_blockscaled(qdy, sdy, qw, sw.t(), fg.FP8_SB_BLOCK128x128)
+    torch.cuda.synchronize()
+    qa_r, sa_r, qw_r, sw_r = dgrad_operands(orc, T, Cin, Cout, seed=41)
+    ref = orc.gemm_blockscaled(qa_r, sa_r, qw_r, np.ascontiguousarray(sw_r.T), orc.SB_BLOCK128x128)
+    gu.assert_gemm_close(gu.host_bf16_as_f64(C), ref, "dgrad end to end")
+
+
 # ---------------------------------------------------------------- grouped --
 
 def moe_operands(orc, counts, N, K, seed, threads=None):
@@ -222,6 +258,19 @@ def test_wgrad_full_workload_sampled(orc, threads):
     got = gu.host_bf16_as_f64(C[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()])
     ref = orc.gemm_blockscaled_sample(qa, sa, qbt, sb, orc.SB_COL128x1, ms, ns, threads=threads)
     gu.assert_gemm_close(got, ref, "wgrad full workload")
+
+
+def test_dgrad_full_workload_sampled(orc, threads):
+    T, Cin, Cout = 8192, 7168, 18432
+    qa, sa, qw, sw = dgrad_operands(orc, T, Cin, Cout, seed=6, threads=threads)
+    C = fg.fp8_gemm_blockscaled(gu.dev(qa), scales_dev(sa, "mn"), gu.dev(qw), gu.dev(sw).t(),
+                                fg.FP8_SB_BLOCK128x128)
+    torch.cuda.synchronize()
+    ms, ns = sample_positions(T, Cin, 4096, 14)
+    got = gu.host_bf16_as_f64(C[torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()])
+    sbT = np.ascontiguousarray(sw.T)
+    ref = orc.gemm_blockscaled_sample(qa, sa, qw, sbT, orc.SB_BLOCK128x128, ms, ns, threads=threads)
+    gu.assert_gemm_close(got, ref, "dgrad full workload")
 
 
 def test_moe_full_workload_sampled(orc, threads):
