@@ -427,6 +427,19 @@ def dist_setup(args):
     return world, rank, local
 
 
+def max_over_ranks(value, world, device):
+    """The largest of every rank's `value` (a time in ms); `value` itself when
+    running alone.  All ranks must call it; the reduction runs on `device`
+    (the rank's GPU under NCCL, the CPU under gloo)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, world, rank):
     """The CPU oracle as the reference arm: rank 0 only, bounded samples."""
     if rank != 0:
@@ -514,11 +527,7 @@ def main():
     clk = clocks.stop()
     if world > 1:
         dist.barrier()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world, device)
     status = fg.fp8_get_device_status(reset=True)
     ms_step = ms_total / args.steps
     value = world * total_flops / (ms_step * 1e-3) / 1e12
@@ -627,11 +636,7 @@ def run_e2e(args, wl, step, stream, total_flops, world, device):
             one()
         e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     ms_step = ms / args.e2e_steps
     # restore the device-resident inputs used by later legs
     step.load_inputs(wl)

@@ -38,7 +38,8 @@ __all__ = [
     "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_batched",
     "fp8_requant_1x128_to_128x1",
     "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled",
-    "fp8_get_device_status", "fp8_status_string",
+    "fp8_get_device_status", "fp8_status_string", "fp8_selftest_bounded_wait",
+    "fp8_mma_accumulation_probe",
     "FP8_KMAJOR_NK", "FP8_ROWMAJOR_KN", "FP8_SB_BLOCK128x128", "FP8_SB_COL128x1",
 ]
 
@@ -70,6 +71,8 @@ _SIGNATURES = {
     "fp8_grouped_gemm_blockscaled": [_vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _int, _i64, _i64, _i64,
                                      _vp, _i64, _vp],
     "fp8_get_device_status": [_vp, ctypes.POINTER(ctypes.c_int32), _int],
+    "fp8_selftest_bounded_wait": [ctypes.c_uint64, _vp],
+    "fp8_mma_accumulation_probe": [_vp, _vp, _i64, _vp, _vp],
     "fp8_status_string": [_int],
     "fp8fg_version": [],
 }
@@ -284,3 +287,25 @@ def fp8_get_device_status(reset=True, stream=None) -> int:
     _check(capi().fp8_get_device_status(_stream(stream), ctypes.byref(v), 1 if reset else 0),
            "fp8_get_device_status")
     return int(v.value)
+
+
+def fp8_selftest_bounded_wait(timeout_ns=1000000, stream=None):
+    """Run the bounded-wait self-test kernel (a wait that nothing satisfies);
+    afterwards the device status word holds FP8_ERR_DEVICE_TIMEOUT (5)."""
+    _check(capi().fp8_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "fp8_selftest_bounded_wait")
+
+
+def fp8_mma_accumulation_probe(A, B, out=None, *, stream=None):
+    """D fp32 [128, 256] = A [128, K] x B [256, K]^T over E4M3 codes (uint8,
+    dense), accumulated over the whole K in tensor memory (no promotion)."""
+    _need_cuda(A, B)
+    if A.dtype != torch.uint8 or B.dtype != torch.uint8 or not (A.is_contiguous() and B.is_contiguous()):
+        raise TypeError("A and B must be contiguous uint8 code matrices")
+    if A.shape[0] != 128 or B.shape[0] != 256 or A.shape[1] != B.shape[1]:
+        raise ValueError("A must be [128, K] and B [256, K]")
+    if out is None:
+        out = torch.empty((128, 256), dtype=torch.float32, device=A.device)
+    _need_cuda(out)
+    _check(capi().fp8_mma_accumulation_probe(_ptr(A), _ptr(B), A.shape[1], _ptr(out), _stream(stream)),
+           "fp8_mma_accumulation_probe")
+    return out

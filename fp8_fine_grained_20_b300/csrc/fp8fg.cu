@@ -11,6 +11,7 @@
 
 #include "../../include/fp8fg.h"
 #include "gemm.cuh"
+#include "probe.cuh"
 #include "quant.cuh"
 
 namespace {
@@ -167,6 +168,17 @@ fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const ui
     return launch_status();
 }
 
+// Self-test of the bounded device wait: one thread waits on an mbarrier that
+// nothing arrives on; when the bound expires it records the timeout status.
+__global__ void k_selftest_bounded_wait(uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0, nullptr, timeout_ns)) record_status(kStatusTimeout);
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -199,6 +211,27 @@ fp8_status_t fp8_get_device_status(void* stream, int32_t* out, int reset) {
         if (cudaMemcpyToSymbol(fp8fg::g_fp8_device_status, &zero, sizeof(int)) != cudaSuccess) return FP8_ERR_CUDA;
     }
     return FP8_OK;
+}
+
+fp8_status_t fp8_selftest_bounded_wait(uint64_t timeout_ns, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > 1000000000ull) return FP8_ERR_ARG;
+    k_selftest_bounded_wait<<<1, 32, 0, as_stream(stream)>>>(timeout_ns);
+    return launch_status();
+}
+
+fp8_status_t fp8_mma_accumulation_probe(const uint8_t* A, const uint8_t* B, int64_t K, float* D, void* stream) {
+    if (K <= 0 || K % 128 || K > (int64_t(1) << 24)) return FP8_ERR_SHAPE;
+    if (!A || !B || !D) return FP8_ERR_NULL;
+    if (!aligned16(A) || !aligned16(B) || (reinterpret_cast<uintptr_t>(D) & 3u)) return FP8_ERR_ALIGN;
+    static int smem_ok[kMaxDevices] = {0};
+    const int dev = current_device();
+    if (!allow_smem(probe::k_mma_accumulation_probe, probe::SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
+    CUtensorMap tmA, tmB;
+    if (!make_kmajor_map(&tmA, A, probe::BM, K, K, probe::BM)) return FP8_ERR_CUDA;
+    if (!make_kmajor_map(&tmB, B, probe::BN, K, K, probe::BN)) return FP8_ERR_CUDA;
+    probe::k_mma_accumulation_probe<<<1, 128, probe::SMEM, as_stream(stream)>>>(tmA, tmB,
+                                                                              static_cast<int>(K / 128), D);
+    return launch_status();
 }
 
 fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,

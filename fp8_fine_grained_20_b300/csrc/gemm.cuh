@@ -391,14 +391,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
         const int row = quarter * 32 + lane;    // row of this CTA's 128-row half
-        uint32_t it = 0, slot = 0, sph = 0, stage = 0, phase = 0;
+        uint32_t it = 0;   // K-blocks promoted so far; every ring position derives from it
         bool ok = true;
         for (int t = pair; ok && t < num_tiles; t += n_pairs) {
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
-            for (int kb = 0; kb < p.k_blocks; ++kb) {
+            for (int kb = 0; kb < p.k_blocks; ++kb, ++it) {
                 const uint32_t buf = it & 1u;
+                const uint32_t slot = it % SSLOTS, sph = (it / SSLOTS) & 1u;
+                const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
                 const bool ready = mbar_wait(&sfull[slot], sph, abort_flag) &&
                                    mbar_wait(&done[stage], phase, abort_flag);
                 if (!__all_sync(0xffffffffu, ready)) {  // warp-uniform: tcgen05.ld is .sync.aligned
@@ -429,15 +431,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 promote32<SBK, 96>(acc, r1, sc, sa, sbv);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[slot]);
-                ++it;
-                if (++slot == SSLOTS) {
-                    slot = 0;
-                    sph ^= 1u;
-                }
-                if (++stage == STAGES) {
-                    stage = 0;
-                    phase ^= 1u;
-                }
             }
             if (!ok) break;
             const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);

@@ -189,6 +189,29 @@ fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda,
                                           void* stream);
 
 /*
+ * Tensor-core accumulation probe (why-be.why-be.co.kr post 55081: the
+ * previous generation's FP8 tensor cores keep about 14 bits when they
+ * accumulate, hence the promotion every 128 K).  Computes
+ *   D[m][n] = sum_{k < K} decode(A[m][k]) * decode(B[n][k])   (no scales)
+ * for m < 128, n < 256 with tcgen05 FP8 MMAs accumulating the whole K in
+ * tensor memory (no promotion), and writes D as fp32 [128][256] (row-major).
+ *   A  E4M3 codes [128][K], dense (row stride K);  B  E4M3 codes [256][K], dense
+ * Requires 128 <= K <= 2^24, K % 128 == 0.  One CTA; meant for measurements,
+ * not speed.
+ */
+fp8_status_t fp8_mma_accumulation_probe(const uint8_t* A, const uint8_t* B, int64_t K, float* D, void* stream);
+
+/*
+ * Self-test of the library's bounded device waits (no counterpart on the
+ * pages).  Launches one thread that waits on a shared-memory mbarrier which
+ * nothing ever arrives on, with the same bounded wait the kernels use; after
+ * timeout_ns (1 ns .. 1 s) it gives up, records FP8_ERR_DEVICE_TIMEOUT in the
+ * device status word and returns, leaving the context usable.  Read the result
+ * with fp8_get_device_status().  FP8_ERR_ARG for a timeout outside the range.
+ */
+fp8_status_t fp8_selftest_bounded_wait(uint64_t timeout_ns, void* stream);
+
+/*
  * Device status word.  Waits for `stream`, copies the status word of the
  * current device into *out (FP8_OK or the first FP8_ERR_DEVICE_* recorded since
  * the last reset) and, if reset != 0, clears it.  Returns FP8_ERR_CUDA if the
