@@ -20,6 +20,8 @@ Functions (same names as the C entry points):
 * ``fp8_gemm_blockscaled(A, sA, B, sB, sb_kind)`` -- bf16 [M, N]; FP32
   promotion every 128 K with both scales applied (why-be.why-be.co.kr post
   55081, Figure 7(b))
+* ``fp8_gemm_blockscaled_q1x128(A, sA, B, sB, sb_kind)`` -- the same GEMM with
+  its bf16 output 1x128-quantized in the epilogue -> (codes, scales)
 * ``fp8_grouped_gemm_blockscaled(A, sA, B, sB, offsets)`` -- MoE experts
   (xn--jj0bz6z98ct0a29q.com post 362465: FP8-dispatched activations)
 
@@ -37,7 +39,7 @@ __all__ = [
     "FP8Error", "capi", "library_path",
     "fp8_quant_act_1x128", "fp8_quant_w_128x128", "fp8_quant_w_128x128_batched",
     "fp8_requant_1x128_to_128x1",
-    "fp8_gemm_blockscaled", "fp8_grouped_gemm_blockscaled",
+    "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_q1x128", "fp8_grouped_gemm_blockscaled",
     "fp8_get_device_status", "fp8_status_string", "fp8_selftest_bounded_wait",
     "fp8_mma_accumulation_probe",
     "FP8_KMAJOR_NK", "FP8_ROWMAJOR_KN", "FP8_SB_BLOCK128x128", "FP8_SB_COL128x1",
@@ -68,6 +70,8 @@ _SIGNATURES = {
                                    _vp],
     "fp8_gemm_blockscaled": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
                              _i64, _i64, _i64, _vp],
+    "fp8_gemm_blockscaled_q1x128": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
+                                    _vp, _i64, _i64, _i64, _i64, _i64, _vp],
     "fp8_grouped_gemm_blockscaled": [_vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _int, _i64, _i64, _i64,
                                      _vp, _i64, _vp],
     "fp8_get_device_status": [_vp, ctypes.POINTER(ctypes.c_int32), _int],
@@ -254,6 +258,31 @@ def fp8_gemm_blockscaled(A, sA, B, sB, sb_kind=FP8_SB_BLOCK128x128, out=None, *,
                                        int(sb_kind), _ptr(out), out.stride(0), M, N, K, _stream(stream)),
            "fp8_gemm_blockscaled")
     return out
+
+
+def fp8_gemm_blockscaled_q1x128(A, sA, B, sB, sb_kind=FP8_SB_BLOCK128x128, q=None, s=None, *,
+                                scale_layout="mn", stream=None):
+    """fp8_gemm_blockscaled whose bf16 output is 1x128-quantized in the epilogue.
+    Returns (q uint8 [M, N], s float32 logical [M, N/128])."""
+    _need_cuda(A, sA, B, sB)
+    _row_major(A, "A")
+    _row_major(B, "B")
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("A and B must share K")
+    if q is None:
+        q = torch.empty((M, N), dtype=torch.uint8, device=A.device)
+    if s is None:
+        s = _scale_out(M, N // 128, scale_layout, A.device)
+    _need_cuda(q, s)
+    _row_major(q, "q")
+    _check(capi().fp8_gemm_blockscaled_q1x128(_ptr(A), A.stride(0), _ptr(sA), sA.stride(0), sA.stride(1),
+                                              _ptr(B), B.stride(0), _ptr(sB), sB.stride(0), sB.stride(1),
+                                              int(sb_kind), _ptr(q), q.stride(0), _ptr(s), s.stride(0),
+                                              s.stride(1), M, N, K, _stream(stream)),
+           "fp8_gemm_blockscaled_q1x128")
+    return q, s
 
 
 def fp8_grouped_gemm_blockscaled(A, sA, B, sB, offsets, out=None, *, stream=None):

@@ -116,14 +116,15 @@ bool allow_smem(K kernel, size_t bytes, int dev, int* done) {
     return true;
 }
 
-template <int SBK, bool GROUPED>
+template <int SBK, bool GROUPED, bool QOUT = false>
 fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const uint8_t* B, int64_t ldb,
-                         int64_t b_rows, const gemm::Args& args, cudaStream_t stream) {
+                         int64_t b_rows, const gemm::Args& args, cudaStream_t stream,
+                         const gemm::QArgs& qargs = gemm::QArgs{}) {
     static int attr_set[kMaxDevices] = {0};
     static int max_pairs[kMaxDevices] = {0};
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
-    auto kernel = gemm::k_gemm_blockscaled<SBK, GROUPED>;
+    auto kernel = gemm::k_gemm_blockscaled<SBK, GROUPED, QOUT>;
     const size_t smem = GROUPED ? gemm::SMEM_GROUPED : gemm::SMEM_PLAIN;
 
     cudaLaunchConfig_t cfg = {};
@@ -161,7 +162,7 @@ fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const ui
     const int64_t tiles = pair_rows * args.n_blocks;
     const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(tiles, max_pairs[dev]));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args, qargs) != cudaSuccess) {
         cudaGetLastError();
         return FP8_ERR_CUDA;
     }
@@ -354,20 +355,29 @@ fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, 
     return launch_status();
 }
 
-fp8_status_t fp8_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
-                                  int64_t sa_stride_kb, const uint8_t* B, int64_t ldb, const float* sB,
-                                  int64_t sb_stride_kb, int64_t sb_stride_n, int sb_kind, uint16_t* C, int64_t ldc,
-                                  int64_t M, int64_t N, int64_t K, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Validation and launch shared by the bf16 and the quantizing epilogue.
+fp8_status_t gemm_entry(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
+                        const uint8_t* B, int64_t ldb, const float* sB, int64_t sb_stride_kb, int64_t sb_stride_n,
+                        int sb_kind, uint16_t* C, int64_t ldc, uint8_t* Cq, int64_t ldcq, float* sC,
+                        int64_t sc_stride_m, int64_t sc_stride_nb, int64_t M, int64_t N, int64_t K, bool qout,
+                        cudaStream_t stream) {
     if (sb_kind != FP8_SB_BLOCK128x128 && sb_kind != FP8_SB_COL128x1) return FP8_ERR_ARG;
     if (M < 0 || N < 0 || K < 0 || M % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
     if (M == 0 || N == 0) return FP8_OK;
     if (K == 0) return FP8_ERR_SHAPE;
-    if (!A || !sA || !B || !sB || !C) return FP8_ERR_NULL;
-    if (lda < K || ldb < K || ldc < N || sa_stride_m < 0 || sa_stride_kb < 0 || sb_stride_kb < 0 ||
-        sb_stride_n < 0)
+    if (!A || !sA || !B || !sB || (qout ? (!Cq || !sC) : !C)) return FP8_ERR_NULL;
+    if (lda < K || ldb < K || sa_stride_m < 0 || sa_stride_kb < 0 || sb_stride_kb < 0 || sb_stride_n < 0)
         return FP8_ERR_ARG;
-    if (!aligned16(A) || !aligned16(B) || !aligned16(C) || lda % 16 || ldb % 16 || (ldc * 2) % 16 ||
-        (reinterpret_cast<uintptr_t>(sA) & 3u) || (reinterpret_cast<uintptr_t>(sB) & 3u))
+    if (qout ? (ldcq < N || sc_stride_m < 0 || sc_stride_nb < 0) : ldc < N) return FP8_ERR_ARG;
+    if (!aligned16(A) || !aligned16(B) || lda % 16 || ldb % 16 || (reinterpret_cast<uintptr_t>(sA) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sB) & 3u))
+        return FP8_ERR_ALIGN;
+    if (qout ? (!aligned16(Cq) || ldcq % 16 || (reinterpret_cast<uintptr_t>(sC) & 3u))
+             : (!aligned16(C) || (ldc * 2) % 16))
         return FP8_ERR_ALIGN;
     if (M / 128 * ceil_div(N, gemm::BN) > INT32_MAX || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX)
         return FP8_ERR_SHAPE;
@@ -390,9 +400,35 @@ fp8_status_t fp8_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA
     a.sb_cols = static_cast<int>(sb_kind == FP8_SB_COL128x1 ? N : N / 128);
     a.offsets = nullptr;
     a.G = 0;
-    if (sb_kind == FP8_SB_COL128x1)
-        return launch_gemm<gemm::SB_COL, false>(A, lda, M, B, ldb, N, a, as_stream(stream));
-    return launch_gemm<gemm::SB_BLOCK, false>(A, lda, M, B, ldb, N, a, as_stream(stream));
+    if (qout) {
+        const gemm::QArgs q{Cq, ldcq, sC, sc_stride_m, sc_stride_nb};
+        if (sb_kind == FP8_SB_COL128x1)
+            return launch_gemm<gemm::SB_COL, false, true>(A, lda, M, B, ldb, N, a, stream, q);
+        return launch_gemm<gemm::SB_BLOCK, false, true>(A, lda, M, B, ldb, N, a, stream, q);
+    }
+    if (sb_kind == FP8_SB_COL128x1) return launch_gemm<gemm::SB_COL, false>(A, lda, M, B, ldb, N, a, stream);
+    return launch_gemm<gemm::SB_BLOCK, false>(A, lda, M, B, ldb, N, a, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8_status_t fp8_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
+                                  int64_t sa_stride_kb, const uint8_t* B, int64_t ldb, const float* sB,
+                                  int64_t sb_stride_kb, int64_t sb_stride_n, int sb_kind, uint16_t* C, int64_t ldc,
+                                  int64_t M, int64_t N, int64_t K, void* stream) {
+    return gemm_entry(A, lda, sA, sa_stride_m, sa_stride_kb, B, ldb, sB, sb_stride_kb, sb_stride_n, sb_kind, C, ldc,
+                      nullptr, 0, nullptr, 0, 0, M, N, K, false, as_stream(stream));
+}
+
+fp8_status_t fp8_gemm_blockscaled_q1x128(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
+                                         int64_t sa_stride_kb, const uint8_t* B, int64_t ldb, const float* sB,
+                                         int64_t sb_stride_kb, int64_t sb_stride_n, int sb_kind, uint8_t* Cq,
+                                         int64_t ldcq, float* sC, int64_t sc_stride_m, int64_t sc_stride_nb,
+                                         int64_t M, int64_t N, int64_t K, void* stream) {
+    return gemm_entry(A, lda, sA, sa_stride_m, sa_stride_kb, B, ldb, sB, sb_stride_kb, sb_stride_n, sb_kind, nullptr,
+                      0, Cq, ldcq, sC, sc_stride_m, sc_stride_nb, M, N, K, true, as_stream(stream));
 }
 
 fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,

@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace fp8fg {
 namespace gemm {
@@ -79,13 +80,22 @@ struct Args {
     const float* sB;
     int64_t sb_skb, sb_sn;
     int64_t sb_group_stride;  // grouped: floats between experts' scale tables
-    uint16_t* C;
+    uint16_t* C;              // bf16 output (plain epilogue)
     int64_t ldc;
     int M, N, K;
     int m_blocks, n_blocks, k_blocks;  // n_blocks: 256-column tiles
     int sb_cols;              // number of valid sB columns: N/128 (block) or N (per column)
     const int32_t* offsets;   // grouped only (device)
     int G;
+};
+
+// Outputs of the quantizing epilogue (a separate kernel parameter, so that
+// the other kernels' parameter block and register allocation are unchanged).
+struct QArgs {
+    uint8_t* Cq;              // codes, row stride ldcq
+    int64_t ldcq;
+    float* sC;                // scales, logical [M][N/128] at sC[m*sc_m + nb*sc_nb]
+    int64_t sc_m, sc_nb;
 };
 
 __device__ const float g_zero_scale = 0.0f;
@@ -185,11 +195,14 @@ __device__ __forceinline__ void signal_abort(volatile int* abort_flag, uint32_t 
 }
 
 // Launch: clusters of 2 CTAs along x, THREADS threads, SMEM_PLAIN or
-// SMEM_GROUPED bytes of dynamic shared memory, one CTA per SM.
-template <int SBK, bool GROUPED>
+// SMEM_GROUPED bytes of dynamic shared memory, one CTA per SM.  QOUT: the
+// epilogue writes the bf16-rounded output 1x128-quantized (codes + scales)
+// instead of bf16; each promotion thread holds exactly one 1x128 group (one
+// row, 128 columns), so the group amax needs no communication.
+template <int SBK, bool GROUPED, bool QOUT = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_blockscaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const Args p) {
+                       const Args p, const QArgs qo) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sm_a = base + OFF_A;
@@ -436,7 +449,27 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
             const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
             const int n0 = tl.nb * BN + half * 128;
-            if (grow < tl.row_end && n0 < p.N) {
+            if (!(grow < tl.row_end && n0 < p.N)) continue;
+            if constexpr (QOUT) {
+                // bf16 rounding of the output as the plain epilogue does, then the
+                // 1x128 quantizer's arithmetic on those bf16 values
+                uint32_t w[64];
+#pragma unroll
+                for (int j = 0; j < 64; ++j) w[j] = pack_bf16x2(acc[2 * j], acc[2 * j + 1]);
+                uint32_t h = 0u;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) h = umax16x2(h, w[j] & 0x7FFF7FFFu);
+                const GroupScale gs = group_scale(hmax_bf16x2_to_f32(h));
+                uint8_t* qrow = qo.Cq + static_cast<int64_t>(grow) * qo.ldcq + n0;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint2 lo = quant8_bf16(make_uint4(w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3]), gs);
+                    const uint2 hi =
+                        quant8_bf16(make_uint4(w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]), gs);
+                    stg_v4(qrow + 16 * c, make_uint4(lo.x, lo.y, hi.x, hi.y));
+                }
+                qo.sC[static_cast<int64_t>(grow) * qo.sc_m + static_cast<int64_t>(n0 / 128) * qo.sc_nb] = gs.s;
+            } else {
                 uint16_t* crow = p.C + static_cast<int64_t>(grow) * p.ldc + n0;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {

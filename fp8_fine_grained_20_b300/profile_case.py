@@ -3,7 +3,8 @@
     python -m fp8_fine_grained_20_b300.profile_case KERNEL [--launches N] [--warmup W]
 
 KERNEL is one of quant_act, quant_w, quant_w_moe (32 experts in one batched
-launch), requant, gemm_fprop, gemm_dgrad, gemm_wgrad, grouped_gemm.  The process allocates only what that one call needs (at most
+launch), requant, gemm_fprop, gemm_fprop_q (the forward GEMM with the 1x128
+quantizing epilogue), gemm_dgrad, gemm_wgrad, grouped_gemm.  The process allocates only what that one call needs (at most
 about 2 GB), fills the bf16 inputs on the device with torch's generator
 (N(0,1) activations with 1% of channels x100, N(0, 0.02^2) weights,
 N(0, 1e-3^2) gradients), quantizes them with the library where the kernel
@@ -87,6 +88,12 @@ def setup(kind):
         b, sb = fg.fp8_quant_w_128x128(weight(CIN, COUT, 5))
         c = torch.empty((T, COUT), dtype=torch.bfloat16, device="cuda")
         return lambda: fg.fp8_gemm_blockscaled(a, sa, b, sb, fg.FP8_SB_BLOCK128x128, c)
+    if kind == "gemm_fprop_q":
+        a, sa = fg.fp8_quant_act_1x128(activation(T, CIN, 4))
+        b, sb = fg.fp8_quant_w_128x128(weight(CIN, COUT, 5))
+        q = torch.empty((T, COUT), dtype=torch.uint8, device="cuda")
+        s = torch.empty((COUT // 128, T), dtype=torch.float32, device="cuda").t()
+        return lambda: fg.fp8_gemm_blockscaled_q1x128(a, sa, b, sb, fg.FP8_SB_BLOCK128x128, q, s)
     if kind == "gemm_dgrad":
         a, sa = fg.fp8_quant_act_1x128(weight(T, COUT, 11, 1e-3))
         b, sb = fg.fp8_quant_w_128x128(weight(CIN, COUT, 12), q_layout=fg.FP8_ROWMAJOR_KN)
@@ -114,7 +121,7 @@ def setup(kind):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("kernel", choices=["quant_act", "quant_w", "quant_w_moe", "requant", "gemm_fprop",
-                                      "gemm_dgrad", "gemm_wgrad", "grouped_gemm"])
+                                      "gemm_fprop_q", "gemm_dgrad", "gemm_wgrad", "grouped_gemm"])
     p.add_argument("--launches", type=int, default=1)
     p.add_argument("--warmup", type=int, default=2)
     args = p.parse_args(argv)

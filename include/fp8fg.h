@@ -165,6 +165,27 @@ fp8_status_t fp8_gemm_blockscaled(const uint8_t* A, int64_t lda,
                                   void* stream);
 
 /*
+ * fp8_gemm_blockscaled with a quantizing epilogue: the GEMM's bf16 output
+ * (rounded exactly as fp8_gemm_blockscaled rounds it) is 1x128-quantized in
+ * the epilogue, as fp8_quant_act_1x128 would quantize it, so a GEMM whose
+ * output feeds another FP8 GEMM writes codes and scales instead of bf16
+ * (the pages cache and dispatch FP8 activations: xn--jj0bz6z98ct0a29q.com
+ * post 362465; sunipension.com post 314414, Figure 7(a), 1x128 tiles).
+ *   Cq   E4M3 codes [M][N], row stride ldcq (>= N, multiple of 16)
+ *   sC   fp32 scales, logical [M][N/128]; (m, nb) at sC[m*sc_stride_m + nb*sc_stride_nb]
+ * Every other argument, requirement and status is as in fp8_gemm_blockscaled.
+ */
+fp8_status_t fp8_gemm_blockscaled_q1x128(const uint8_t* A, int64_t lda,
+                                         const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
+                                         const uint8_t* B, int64_t ldb,
+                                         const float* sB, int64_t sb_stride_kb, int64_t sb_stride_n,
+                                         int sb_kind,
+                                         uint8_t* Cq, int64_t ldcq,
+                                         float* sC, int64_t sc_stride_m, int64_t sc_stride_nb,
+                                         int64_t M, int64_t N, int64_t K,
+                                         void* stream);
+
+/*
  * Grouped block-scaled FP8 GEMM for a variable-size MoE expert batch
  * (xn--jj0bz6z98ct0a29q.com post 362465: activations dispatched in FP8).
  * Expert g owns rows [off[g], off[g+1]) of A and C and multiplies them by B_g:

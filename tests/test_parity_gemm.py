@@ -299,3 +299,53 @@ def test_moe_full_workload_sampled(orc, threads):
         pad0, pad1 = int(inp.offsets[g] + inp.counts[g]), int(inp.offsets[g + 1])
         if pad1 > pad0:
             assert float(C[pad0:pad1].float().abs().max()) == 0.0
+
+
+# ------------------------------------------------------ quantizing epilogue --
+
+def _bf16_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("kind,M,N,K", [("block", 256, 512, 384), ("block", 384, 384, 1024),
+                                         ("col", 256, 384, 256), ("block", 128, 128, 128)])
+def test_gemm_q1x128_epilogue_matches_oracle_quantizer(orc, kind, M, N, K):
+    """Codes and scales of the quantizing epilogue equal the oracle's 1x128
+    quantization of the same GEMM's bf16 output, bit for bit; the bf16 GEMM
+    itself is checked against the FP64 oracle."""
+    if kind == "block":
+        qa, sa, qbt, sb = fprop_operands(orc, M, N, K, seed=M + N + K)
+        sb_kind, osk = fg.FP8_SB_BLOCK128x128, orc.SB_BLOCK128x128
+    else:
+        qa, sa, qbt, sb = wgrad_operands(orc, K, M, N, seed=M + N + K)
+        sb_kind, osk = fg.FP8_SB_COL128x1, orc.SB_COL128x1
+    A, B, sA, sB = gu.dev(qa), gu.dev(qbt), scales_dev(sa, "mn"), gu.dev(sb)
+    C = fg.fp8_gemm_blockscaled(A, sA, B, sB, sb_kind)
+    q, s = fg.fp8_gemm_blockscaled_q1x128(A, sA, B, sB, sb_kind)
+    torch.cuda.synchronize()
+    gu.assert_gemm_close(gu.host_bf16_as_f64(C), orc.gemm_blockscaled(qa, sa, qbt, sb, osk), "bf16 GEMM")
+    q_ref, s_ref = orc.quant_act_1x128(_bf16_bits(C))
+    assert np.array_equal(gu.host(q), q_ref)
+    assert np.array_equal(gu.host(s).view(np.uint32), s_ref.view(np.uint32))
+
+
+def test_gemm_q1x128_epilogue_full_workload_matches_unfused():
+    """Forward GEMM at full size: the fused epilogue equals GEMM -> 1x128
+    quantizer on the GPU, every code and scale."""
+    gu.cuda_or_skip()
+    M, N, K = 8192, 18432, 7168
+    g = torch.Generator(device="cuda")
+    g.manual_seed(5)
+    x = torch.randn((M, K), generator=g, device="cuda").to(torch.bfloat16)
+    w = (torch.randn((K, N), generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    qa, sa = fg.fp8_quant_act_1x128(x)
+    qb, sb = fg.fp8_quant_w_128x128(w)
+    del x, w
+    C = fg.fp8_gemm_blockscaled(qa, sa, qb, sb)
+    q_ref, s_ref = fg.fp8_quant_act_1x128(C)
+    del C
+    q, s = fg.fp8_gemm_blockscaled_q1x128(qa, sa, qb, sb)
+    torch.cuda.synchronize()
+    assert torch.equal(q, q_ref)
+    assert torch.equal(s.contiguous().view(torch.int32), s_ref.contiguous().view(torch.int32))
+    assert fg.fp8_get_device_status(reset=True) == 0
