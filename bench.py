@@ -22,7 +22,8 @@ FP8 training step of a large MoE transformer layer:
 for the MoE) divided by the step time, summed over ranks: whole-step TFLOP/s,
 quantizers included.  Inputs live in HBM before the timed region; every input
 is larger than L2 or is followed by larger traffic.  `e2e` repeats the step
-with the inputs copied from pinned host memory and the outputs read back.
+with the inputs copied from pinned host memory and the outputs read back, the
+copies of neighbouring steps overlapping the kernels (two buffer sets).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -63,7 +64,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=300)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=6)
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
@@ -411,10 +412,19 @@ def cpu_oracle_sample(wl, frac, threads=1):
     return t_total, "; ".join(parts), est
 
 
-def calibrate_frac(wl, target_seconds):
+def oracle_threads():
+    """Host threads for the oracle: every core the process may use (at most 32)."""
+    try:
+        n = len(os.sched_getaffinity(0))
+    except AttributeError:
+        n = os.cpu_count() or 1
+    return max(1, min(32, n))
+
+
+def calibrate_frac(wl, target_seconds, threads=1):
     """Fraction of the step whose oracle run takes about `target_seconds`."""
     probe = 2e-5
-    t, _, est = cpu_oracle_sample(wl, probe)
+    t, _, est = cpu_oracle_sample(wl, probe, threads=threads)
     return min(1.0, max(1e-7, target_seconds / max(est, 1e-9))), est
 
 
@@ -447,13 +457,14 @@ def run_reference(args, world, rank):
     wl = Workload()
     flops = sum(wl.gemm_flops().values())
     per_step = max(0.05, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
-    frac, est_full = calibrate_frac(wl, per_step)
+    threads = oracle_threads()
+    frac, est_full = calibrate_frac(wl, per_step, threads)
     for _ in range(args.warmup):
-        cpu_oracle_sample(wl, frac)
+        cpu_oracle_sample(wl, frac, threads=threads)
     samples, ests = [], []
     desc = ""
     for _ in range(args.steps):
-        t, desc, est = cpu_oracle_sample(wl, frac)
+        t, desc, est = cpu_oracle_sample(wl, frac, threads=threads)
         samples.append(t)
         ests.append(est)
     est_step = statistics.mean(ests)
@@ -464,7 +475,7 @@ def run_reference(args, world, rank):
         "sample_ms_per_step": statistics.mean(samples) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": wl.describe(),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": "fraction %.3g of each kernel's work per step: %s" % (frac, desc)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -570,9 +581,10 @@ def main():
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        frac, _ = calibrate_frac(wl, args.cpu_seconds)
-        secs, desc, est = cpu_oracle_sample(wl, frac)
-        cpu = {"value": total_flops / est / 1e12, "unit": UNIT, "cores": 1, "kind": "oracle",
+        threads = oracle_threads()
+        frac, _ = calibrate_frac(wl, args.cpu_seconds, threads)
+        secs, desc, est = cpu_oracle_sample(wl, frac, threads=threads)
+        cpu = {"value": total_flops / est / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": "fraction %.3g of every kernel's work (%s), %.1f s measured, extrapolated to the "
                          "whole step" % (frac, desc, secs)}
 
@@ -596,52 +608,81 @@ def main():
 
 
 def run_e2e(args, wl, step, stream, total_flops, world, device):
+    """The step through the public API with host buffers: every step copies
+    its bf16 inputs from pinned host memory and its four bf16 outputs back.
+    Two device buffer sets alternate, so the host-to-device copies of step
+    i + 1 (copy stream), the kernels of step i (compute stream) and the
+    device-to-host copies of step i - 1 (a third stream) overlap; events keep
+    each buffer set's copies and kernels in order.  All copies of all steps
+    are inside the timed region."""
     import torch
-    import torch.distributed as dist
 
     def pinned(a, dtype=None):
         t = torch.from_numpy(np.ascontiguousarray(a))
         if dtype is not None:
             t = t.view(dtype)
         return t.pin_memory()
-    h_in = [(pinned(wl.x.view(np.int16), torch.bfloat16), step.x),
-            (pinned(wl.w.view(np.int16), torch.bfloat16), step.w),
-            (pinned(wl.dy.view(np.int16), torch.bfloat16), step.dy),
-            (pinned(wl.moe_x.view(np.int16), torch.bfloat16), step.moe_x),
-            (pinned(wl.moe_w.view(np.int16), torch.bfloat16), step.moe_w),
-            (pinned(wl.moe_offsets), step.moe_off)]
-    h_out = [(step.y, torch.empty(step.y.shape, dtype=step.y.dtype).pin_memory()),
-             (step.dx, torch.empty(step.dx.shape, dtype=step.dx.dtype).pin_memory()),
-             (step.dw, torch.empty(step.dw.shape, dtype=step.dw.dtype).pin_memory()),
-             (step.moe_y, torch.empty(step.moe_y.shape, dtype=step.moe_y.dtype).pin_memory())]
-    h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
-    d2h = sum(h.numel() * h.element_size() for _, h in h_out)
+    h_in = [pinned(wl.x.view(np.int16), torch.bfloat16), pinned(wl.w.view(np.int16), torch.bfloat16),
+            pinned(wl.dy.view(np.int16), torch.bfloat16), pinned(wl.moe_x.view(np.int16), torch.bfloat16),
+            pinned(wl.moe_w.view(np.int16), torch.bfloat16), pinned(wl.moe_offsets)]
+    sets = [step, DeviceStep(wl, device)]
 
-    def one():
-        for h, d in h_in:
-            d.copy_(h, non_blocking=True)
-        step.run(stream)
-        for d, h in h_out:
-            h.copy_(d, non_blocking=True)
-    with torch.cuda.stream(stream):
-        one()
+    def dev_in(st):
+        return [st.x, st.w, st.dy, st.moe_x, st.moe_w, st.moe_off]
+
+    def dev_out(st):
+        return [st.y, st.dx, st.dw, st.moe_y]
+    h_out = [[torch.empty(d.shape, dtype=d.dtype).pin_memory() for d in dev_out(st)] for st in sets]
+    h2d = sum(h.numel() * h.element_size() for h in h_in)
+    d2h = sum(h.numel() * h.element_size() for h in h_out[0])
+    s_h2d = torch.cuda.Stream(device=device)
+    s_d2h = torch.cuda.Stream(device=device)
+    ev = [{k: torch.cuda.Event() for k in ("h2d", "compute", "d2h")} for _ in sets]
+
+    def one(i):
+        j = i % 2
+        st, e = sets[j], ev[j]
+        if i >= 2:
+            s_h2d.wait_event(e["compute"])          # the kernels of step i - 2 no longer read these inputs
+        with torch.cuda.stream(s_h2d):
+            for h, d in zip(h_in, dev_in(st)):
+                d.copy_(h, non_blocking=True)
+        e["h2d"].record(s_h2d)
+        stream.wait_event(e["h2d"])
+        if i >= 2:
+            stream.wait_event(e["d2h"])             # step i - 2's outputs are on the host
+        st.run(stream)
+        e["compute"].record(stream)
+        s_d2h.wait_event(e["compute"])
+        with torch.cuda.stream(s_d2h):
+            for d, h in zip(dev_out(st), h_out[j]):
+                h.copy_(d, non_blocking=True)
+        e["d2h"].record(s_d2h)
+
+    for i in range(2):                               # warm-up of both buffer sets
+        one(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
+        import torch.distributed as dist
         dist.barrier()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            one()
-        e1.record(stream)
+    e0.record(s_h2d)
+    for i in range(args.e2e_steps):
+        one(i)
+    stream.wait_event(ev[(args.e2e_steps - 1) % 2]["d2h"])
+    stream.wait_event(ev[args.e2e_steps % 2]["d2h"])
+    e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     ms_step = ms / args.e2e_steps
+    del sets[1]
+    torch.cuda.empty_cache()
     # restore the device-resident inputs used by later legs
     step.load_inputs(wl)
     return {"value": world * total_flops / (ms_step * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms_step,
-            "steps": args.e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "steps": args.e2e_steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "two device buffer sets; host-to-device, kernels and device-to-host on three streams"}
 
 
 if __name__ == "__main__":
