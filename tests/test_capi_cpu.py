@@ -116,3 +116,51 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(4, 128, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         fg.fp8_quant_act_1x128(x)
+
+
+def test_batched_weight_quant_rejections(lib):
+    f = lib.fp8_quant_w_128x128_batched
+    K, N = 256, 384
+    ok = [A16, 3, K, N, N, K * N, A16b, K, N * K, 0, A16, 3, 1, 6, NULL]
+    bad = list(ok); bad[1] = -1
+    assert f(*bad) == 3                                   # negative G
+    bad = list(ok); bad[1] = 0
+    assert f(*bad) == 0                                   # no experts: nothing launched
+    bad = list(ok); bad[5] = K * N - 8
+    assert f(*bad) == 6                                   # experts overlap
+    bad = list(ok); bad[5] = K * N + 4
+    assert f(*bad) == 2                                   # expert stride not a multiple of 16 bytes
+    bad = list(ok); bad[6] = NULL
+    assert f(*bad) == 1
+    bad = list(ok); bad[9] = 7
+    assert f(*bad) == 6                                   # layout
+    bad = list(ok); bad[2] = 200
+    assert f(*bad) == 3                                   # K % 128
+
+
+def test_quantizing_gemm_rejections(lib):
+    f = lib.fp8_gemm_blockscaled_q1x128
+    ok = [A16, 256, A16, 1, 256, A16b, 256, A16, 2, 1, 0, A16b, 256, A16, 1, 256, 256, 256, 256, NULL]
+    bad = list(ok); bad[11] = NULL
+    assert f(*bad) == 1                                   # codes
+    bad = list(ok); bad[13] = NULL
+    assert f(*bad) == 1                                   # scales
+    bad = list(ok); bad[12] = 128
+    assert f(*bad) == 6                                   # ldcq < N
+    bad = list(ok); bad[12] = 264
+    assert f(*bad) == 2                                   # ldcq not a multiple of 16
+    bad = list(ok); bad[13] = ctypes.c_void_p(0x10002)
+    assert f(*bad) == 2                                   # misaligned scales
+    bad = list(ok); bad[17] = 200
+    assert f(*bad) == 3                                   # N % 128
+
+
+def test_probe_and_selftest_rejections(lib):
+    probe = lib.fp8_mma_accumulation_probe
+    assert probe(A16, A16b, 0, A16, NULL) == 3
+    assert probe(A16, A16b, 100, A16, NULL) == 3
+    assert probe(NULL, A16b, 128, A16, NULL) == 1
+    assert probe(MIS, A16b, 128, A16, NULL) == 2
+    wait = lib.fp8_selftest_bounded_wait
+    assert wait(0, NULL) == 6
+    assert wait(2_000_000_000, NULL) == 6

@@ -225,6 +225,26 @@ def test_grouped_small_with_empty_and_exact_experts(orc):
         assert np.all(got[r0:offsets[g + 1]] == 0.0)
 
 
+def test_grouped_single_expert(orc):
+    qa, sa, qb, sb, offsets = moe_operands(orc, [300], N=256, K=384, seed=51)
+    ref = orc.grouped_gemm_blockscaled(qa, sa, qb, sb, offsets)
+    C = run_grouped(qa, sa, qb, sb, offsets)
+    gu.assert_gemm_close(gu.host_bf16_as_f64(C[:300]), ref[:300], "single expert")
+    assert float(C[300:].float().abs().max()) == 0.0          # pad rows
+
+
+def test_grouped_all_experts_empty(orc):
+    """Every expert empty: no tile is computed and the output is not written."""
+    gu.cuda_or_skip()
+    qa = np.zeros((128, 256), np.uint8)
+    sa = np.zeros((128, 2), np.float32)
+    qb = np.zeros((3, 256, 256), np.uint8)
+    sb = np.ones((3, 2, 2), np.float32)
+    C = run_grouped(qa, sa, qb, sb, np.zeros(4, np.int32), fill=7.0)
+    assert bool((C == 7.0).all())
+    assert fg.fp8_get_device_status(reset=True) == 0
+
+
 def test_grouped_bad_offsets_report_device_status(orc):
     qa, sa, qb, sb, offsets = moe_operands(orc, [128, 128], N=256, K=128, seed=5)
     bad = offsets.copy()
