@@ -333,11 +333,8 @@ fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, 
     const int sms = sm_count(dev);
     if (sms <= 0) return FP8_ERR_CUDA;
     if (!allow_smem(k_requant_1x128_to_128x1, RQ_SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
-    CUtensorMap tm;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldq)};
-    const cuuint32_t box[2] = {128u, 128u};
-    if (!make_plain_map(&tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, 2, dims, strides, box)) return FP8_ERR_CUDA;
+    CUtensorMap tm;   // 128 x 128 code blocks, 128-byte swizzle
+    if (!make_kmajor_map(&tm, q, M, K, ldq, 128)) return FP8_ERR_CUDA;
     RequantArgs a{};
     a.s = s;
     a.ssm = s_stride_m;

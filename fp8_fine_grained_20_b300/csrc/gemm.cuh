@@ -29,8 +29,9 @@
 //   * warp 2 (both CTAs): scale loader -- cp.async of the K-block's 128 row
 //     scales of this CTA and the tile's B scales into an 8-slot ring;
 //   * warps 4-11 (both CTAs): promotion -- tcgen05.ld of this CTA's 128 x 256
-//     partial (each warp: its 32 TMEM lanes = rows, one 128-column half),
-//     release of the TMEM buffer to the even CTA, acc += partial * sA * sB in
+//     partial (each warp: its 32 TMEM lanes = rows, one 128-column half, in
+//     four 32-column loads, two in flight), release of the TMEM buffer to the
+//     even CTA as soon as the last two loads land, acc += partial * sA * sB in
 //     FP32 registers with packed FP32x2 FMAs, bf16 stores at tile end.
 //   The MMA of K-block kb+1 runs while K-block kb is promoted.
 #pragma once
@@ -149,6 +150,7 @@ __device__ __forceinline__ Tile tile_at(int t, const Args& p, int pair_rows, con
     }
     return x;
 }
+
 
 template <int SBK, int OFF>
 __device__ __forceinline__ void promote32(float (&acc)[128], const uint32_t (&r)[32], float sc, float sa,
@@ -428,19 +430,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN + half * 128;
                 uint32_t r0[32], r1[32];
                 tmem_ld_32cols(taddr + 0, r0);
-                tmem_wait_ld(r0);
                 tmem_ld_32cols(taddr + 32, r1);
+                tmem_wait_ld2(r0, r1);
                 promote32<SBK, 0>(acc, r0, sc, sa, sbv);
-                tmem_wait_ld(r1);
                 tmem_ld_32cols(taddr + 64, r0);
                 promote32<SBK, 32>(acc, r1, sc, sa, sbv);
-                tmem_wait_ld(r0);
                 tmem_ld_32cols(taddr + 96, r1);
-                promote32<SBK, 64>(acc, r0, sc, sa, sbv);
-                tmem_wait_ld(r1);
+                tmem_wait_ld2(r0, r1);
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&tempty[buf]), 0));  // the even CTA's
+                promote32<SBK, 64>(acc, r0, sc, sa, sbv);
                 promote32<SBK, 96>(acc, r1, sc, sa, sbv);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[slot]);

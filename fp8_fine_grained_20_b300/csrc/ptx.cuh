@@ -288,6 +288,20 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                  : "memory");
 }
 
+// tcgen05.wait::ld covers every earlier tcgen05.ld of the thread; this form
+// orders the uses of two register arrays after it.
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&r0)[32], uint32_t (&r1)[32]) {
+    tmem_wait_ld(r0);
+    asm volatile(""
+                 : "+r"(r1[0]), "+r"(r1[1]), "+r"(r1[2]), "+r"(r1[3]), "+r"(r1[4]), "+r"(r1[5]), "+r"(r1[6]),
+                   "+r"(r1[7]), "+r"(r1[8]), "+r"(r1[9]), "+r"(r1[10]), "+r"(r1[11]), "+r"(r1[12]), "+r"(r1[13]),
+                   "+r"(r1[14]), "+r"(r1[15]), "+r"(r1[16]), "+r"(r1[17]), "+r"(r1[18]), "+r"(r1[19]),
+                   "+r"(r1[20]), "+r"(r1[21]), "+r"(r1[22]), "+r"(r1[23]), "+r"(r1[24]), "+r"(r1[25]),
+                   "+r"(r1[26]), "+r"(r1[27]), "+r"(r1[28]), "+r"(r1[29]), "+r"(r1[30]), "+r"(r1[31])
+                 :
+                 : "memory");
+}
+
 // ------------------------------------------- tcgen05, CTA pair (2 SMs) ----
 // A kernel uses either these or the single-CTA forms above, never both.
 

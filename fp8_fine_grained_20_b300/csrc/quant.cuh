@@ -381,28 +381,37 @@ __global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_
 
 // ------------------------------------------- 1x128 -> 128x1 requantizer ----
 //
-// Persistent CTAs (two per SM) over 128 (tokens) x 128 (channels) blocks.  TMA
-// brings each 16 KB code block into an RQ_STAGES-deep ring; the block's 128
-// row scales (any strides) arrive by cp.async on the same mbarrier.  A thread
-// owns 4 adjacent channels (one 4-byte shared load per row; a warp reads a
-// whole 128-byte row) of 16 consecutive rows.  Pass 1 dequantizes (one fp32
-// multiply, xhat = decode(q) * s) into registers and takes the per-channel
-// amax; warps combine through shared memory and one thread per channel derives
-// the 128x1 scale and reciprocal.  Pass 2 quantizes the registers; per channel
-// the 16 codes of the thread's rows (16 contiguous bytes of the transposed
-// output row) go to a shared staging tile (rows skewed by a bank group every
-// 4 rows, so a warp's writes do not conflict), which is then copied out with
-// 16-byte stores, 8 lanes per 128-byte output row.  The sign of every dequantized value is the sign
-// bit of its input code, so the input bytes supply the sign bits.
+// Persistent CTAs (two per SM) of RQ_WARPS warps over 128 (tokens) x 128
+// (channels) blocks.  Warp 0 also feeds an RQ_STAGES-deep ring: TMA brings
+// each 16 KB code block (128-byte swizzle) and cp.async the block's 128 row
+// scales (any strides), both completing on the stage's full barrier; when warp
+// 0 starts block i it refills the stage of block i-1, once every warp has
+// arrived on that stage's empty barrier.  Warp w owns channels 16w..16w+15 of
+// every block, so no data crosses warps and the loop has no block-wide
+// barrier.  Lane (g, c) = (lane / 8, lane % 8) owns channels
+// 16w+2c and 16w+2c+1 of the 32 rows 8a+2g+b (a < 16, b < 2): one 2-byte
+// shared load per row, and the four row groups of a load sit in distinct
+// swizzle classes, so a warp's load touches 32 distinct banks.
+//   Pass 1 dequantizes (xhat = decode(q) * s, one fp32 multiply) into
+// registers and takes each channel's amax over the lane's rows, then over the
+// four row groups by shuffles; the warp then releases the stage.  Lanes g = 0
+// and g = 1 own the scale of channel 2c and 2c+1; every lane receives its two
+// channels' scale and reciprocal by shuffles.
+//   Pass 2 quantizes the registers.  Rows 8a+2g and 8a+2g+1 are adjacent bytes
+// of a transposed output row, so a pair of codes goes to the warp's staging
+// tile ([16 channels][128 tokens]) with one 2-byte store; the tile's 16-byte
+// chunks are XOR-swizzled by channel pair, so the eight channel rows written
+// by one store land in distinct banks.  The warp then copies its 16 output
+// rows out with 16-byte stores, eight lanes per 128-byte row.  The sign bit
+// of every code is that of its dequantized value (the input code's sign, as
+// the row scales are not negative).
 constexpr int RQ_STAGES = 4;
-constexpr int RQ_THREADS = 256;
-constexpr int RQ_WARPS = RQ_THREADS / 32;
-constexpr int RQ_ROWS = 128 / RQ_WARPS;    // rows per thread
+constexpr int RQ_WARPS = 8;                       // 16 channels each
+constexpr int RQ_THREADS = 32 * RQ_WARPS;
 constexpr uint32_t RQ_TILE_BYTES = 128 * 128;
-constexpr uint32_t RQ_STAGE_OUT = 17024;   // >= stage_bytes<2>(), multiple of 128
-static_assert(RQ_STAGE_OUT >= stage_bytes<2>() && RQ_STAGE_OUT % 128 == 0, "requant staging tile");
-constexpr size_t RQ_SMEM = 128 + RQ_STAGES * RQ_TILE_BYTES + RQ_STAGE_OUT + RQ_STAGES * 128 * 4 + RQ_WARPS * 128 * 4 +
-                           3 * 128 * 4 + RQ_STAGES * 8;
+constexpr uint32_t RQ_WSTAGE = 16 * 128;          // one warp's staged output rows
+constexpr size_t RQ_SMEM = 1024 + RQ_STAGES * RQ_TILE_BYTES + RQ_WARPS * RQ_WSTAGE + RQ_STAGES * 128 * 4 +
+                           2 * RQ_STAGES * 8;
 
 struct RequantArgs {
     const float* s;
@@ -414,148 +423,175 @@ struct RequantArgs {
     int MB, KB;
 };
 
+__device__ __forceinline__ uint32_t lds_u16(const void* p) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(smem_addr(p)));
+    return v;
+}
+
+__device__ __forceinline__ void sts_u16(void* p, uint32_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_addr(p)), "h"(static_cast<uint16_t>(v)) : "memory");
+}
+
 __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const __grid_constant__ CUtensorMap tmQ,
                                                                           const RequantArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-    uint8_t* tiles = base;                                                        // [stage][128 m][128 k]
-    uint8_t* out = base + RQ_STAGES * RQ_TILE_BYTES;                              // staged [128 k][128 m]
-    float* sc = reinterpret_cast<float*>(out + RQ_STAGE_OUT);                    // [stage][128] row scales
-    float* red = sc + RQ_STAGES * 128;                                           // [warp][128 channels]
-    float* cs = red + RQ_WARPS * 128;                                                   // channel scale
-    float* cr = cs + 128;                                                        // channel reciprocal
-    int* cm = reinterpret_cast<int*>(cr + 128);                                  // channel mode
-    uint64_t* full = reinterpret_cast<uint64_t*>(cm + 128);
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* tiles = base;                                                  // [stage][128 m][128 k], swizzled
+    uint8_t* stg = tiles + RQ_STAGES * RQ_TILE_BYTES;                       // [warp][16 k][128 m]
+    float* sc = reinterpret_cast<float*>(stg + RQ_WARPS * RQ_WSTAGE);       // [stage][128] row scales
+    uint64_t* full = reinterpret_cast<uint64_t*>(sc + RQ_STAGES * 128);
+    uint64_t* empty = full + RQ_STAGES;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int total = a.MB * a.KB;
 
-    // TMA of the codes (thread 0) and cp.async of the row scales (threads 0-127),
-    // both completing on full[stage]: 1 expect-tx arrival + 128 cp.async arrivals.
-    auto issue = [&](int stage, int blk) {
-        const int mb = blk / a.KB;
-        const int kb = blk - mb * a.KB;
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&full[stage], RQ_TILE_BYTES);
-            tma_load_2d(tiles + stage * RQ_TILE_BYTES, &tmQ, &full[stage], kb * 128, mb * 128);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RQ_STAGES; ++i) {
+            mbar_init(&full[i], 33);   // expect-tx arrival + 32 cp.async arrivals
+            mbar_init(&empty[i], RQ_WARPS);
         }
-        if (tid < 128) {
-            cp_async_4(sc + stage * 128 + tid,
-                       a.s + static_cast<int64_t>(mb * 128 + tid) * a.ssm + static_cast<int64_t>(kb) * a.sskb);
-            cp_async_arrive_noinc(&full[stage]);
-        }
-    };
-    if (tid == 0) {
-        for (int i = 0; i < RQ_STAGES; ++i) mbar_init(&full[i], 129);
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
     }
     __syncthreads();
-    for (int i = 0; i < RQ_STAGES; ++i) {
-        const int blk = blockIdx.x + i * gridDim.x;
-        if (blk < total) issue(i, blk);
+
+    // TMA of the codes (lane 0) and cp.async of the row scales (4 per lane) of
+    // block blk into a stage, both completing on full[stage]: one expect-tx
+    // arrival + 32 cp.async arrivals.  Called by warp 0 only.
+    auto issue = [&](int stage, int blk) {
+        const int mb = blk / a.KB;
+        const int kb = blk - mb * a.KB;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(&full[stage], RQ_TILE_BYTES);
+            tma_load_2d(tiles + stage * RQ_TILE_BYTES, &tmQ, &full[stage], kb * 128, mb * 128);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int r = lane + 32 * j;
+            cp_async_4(sc + stage * 128 + r,
+                       a.s + static_cast<int64_t>(mb * 128 + r) * a.ssm + static_cast<int64_t>(kb) * a.sskb);
+        }
+        cp_async_arrive_noinc(&full[stage]);
+    };
+    if (warp == 0) {
+        for (int i = 0; i < RQ_STAGES; ++i) {
+            const int blk = blockIdx.x + i * gridDim.x;
+            if (blk < total) issue(i, blk);
+        }
     }
 
+    const int w = warp;
+    const int g = lane >> 3;
+    const int c = lane & 7;
+    uint8_t* wst = stg + w * RQ_WSTAGE;
     bool ok = true;
     for (int i = 0;; ++i) {
         const int blk = blockIdx.x + i * gridDim.x;
         if (blk >= total) break;
         const int stage = i % RQ_STAGES;
-        if (!__syncthreads_and(mbar_wait(&full[stage], (i / RQ_STAGES) & 1u, nullptr))) {
-            if (tid == 0) record_status(kStatusTimeout);
+        if (warp == 0 && i > 0) {
+            // refill the stage of block i-1 with block i-1+RQ_STAGES
+            const int64_t nxt = static_cast<int64_t>(blk) + static_cast<int64_t>(RQ_STAGES - 1) * gridDim.x;
+            const int ps = (i - 1) % RQ_STAGES;
+            if (nxt < total) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&empty[ps], ((i - 1) / RQ_STAGES) & 1u, nullptr))) {
+                    ok = false;
+                    break;
+                }
+                issue(ps, static_cast<int>(nxt));
+            }
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (i / RQ_STAGES) & 1u, nullptr))) {
             ok = false;
             break;
         }
         const int mb = blk / a.KB;
         const int kb = blk - mb * a.KB;
         const uint8_t* tile = tiles + stage * RQ_TILE_BYTES;
-        const float* srow = sc + stage * 128 + RQ_ROWS * warp;
+        const float* srow = sc + stage * 128;
 
-        // pass 1: dequantize 16 rows x 4 channels, per-channel amax
-        uint32_t wv[RQ_ROWS];
-        float xv[RQ_ROWS][4];
-        float am[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        // pass 1: dequantize rows 8a+2g+b, channels 2c, 2c+1; per-channel amax
+        float xv[16][4];     // [a][2b + j]
+        float am0 = 0.0f, am1 = 0.0f;
 #pragma unroll
-        for (int rr = 0; rr < RQ_ROWS; ++rr) {
-            wv[rr] = lds_u32(tile + (RQ_ROWS * warp + rr) * 128 + 4 * lane);
-            const float sr = srow[rr];
-            const uint32_t h0 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(wv[rr] & 0xFFFFu));
-            const uint32_t h1 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(wv[rr] >> 16));
+        for (int aa = 0; aa < 16; ++aa) {
+            const int r0 = 8 * aa + 2 * g;
+            // 128-byte swizzle: 16-byte chunk w of row r sits at chunk w ^ (r % 8)
+            const uint32_t lo = lds_u16(tile + r0 * 128 + ((w ^ (2 * g)) << 4) + 2 * c);
+            const uint32_t hi = lds_u16(tile + (r0 + 1) * 128 + ((w ^ (2 * g + 1)) << 4) + 2 * c);
+            const float2 s2 = *reinterpret_cast<const float2*>(srow + r0);
+            const uint32_t h0 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(lo));
+            const uint32_t h1 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(hi));
             const float2 p0 = __fmul2_rn(make_float2(f16_bits_to_f32(h0 & 0xFFFFu), f16_bits_to_f32(h0 >> 16)),
-                                         make_float2(sr, sr));
+                                         make_float2(s2.x, s2.x));
             const float2 p1 = __fmul2_rn(make_float2(f16_bits_to_f32(h1 & 0xFFFFu), f16_bits_to_f32(h1 >> 16)),
-                                         make_float2(sr, sr));
-            xv[rr][0] = p0.x;
-            xv[rr][1] = p0.y;
-            xv[rr][2] = p1.x;
-            xv[rr][3] = p1.y;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) am[c] = fmaxf(am[c], fabsf(xv[rr][c]));
+                                         make_float2(s2.y, s2.y));
+            xv[aa][0] = p0.x;
+            xv[aa][1] = p0.y;
+            xv[aa][2] = p1.x;
+            xv[aa][3] = p1.y;
+            am0 = fmaxf(am0, fmaxf(fabsf(p0.x), fabsf(p1.x)));
+            am1 = fmaxf(am1, fmaxf(fabsf(p0.y), fabsf(p1.y)));
         }
-        *reinterpret_cast<float4*>(red + warp * 128 + 4 * lane) = make_float4(am[0], am[1], am[2], am[3]);
-        __syncthreads();
-        if (tid < 128) {   // one scale computation per channel
-            float m = red[tid];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);   // this warp no longer reads the stage
+        am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, 8));
+        am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, 16));
+        am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 8));
+        am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 16));
+        const GroupScale gs = group_scale((g & 1) ? am1 : am0);   // lane (g, c): channel 2c + (g & 1)
+        if (g < 2)
+            a.sT[static_cast<int64_t>(kb * 128 + 16 * w + 2 * c + g) * a.sTk + static_cast<int64_t>(mb) * a.sTmb] =
+                gs.s;
+        float chs[2], chr[2];
+        int chm[2];
 #pragma unroll
-            for (int w = 1; w < RQ_WARPS; ++w) m = fmaxf(m, red[w * 128 + tid]);
-            const GroupScale g = group_scale(m);
-            cs[tid] = g.s;
-            cr[tid] = g.r;
-            cm[tid] = g.mode;
-            a.sT[static_cast<int64_t>(kb * 128 + tid) * a.sTk + static_cast<int64_t>(mb) * a.sTmb] = g.s;
+        for (int j = 0; j < 2; ++j) {
+            chs[j] = __shfl_sync(0xffffffffu, gs.s, c + 8 * j);
+            chr[j] = __shfl_sync(0xffffffffu, gs.r, c + 8 * j);
+            chm[j] = __shfl_sync(0xffffffffu, gs.mode, c + 8 * j);
         }
-        __syncthreads();
 
-        // pass 2: quantize each channel's 16 rows and write them transposed
-        const float4 s4 = *reinterpret_cast<const float4*>(cs + 4 * lane);
-        const float4 r4 = *reinterpret_cast<const float4*>(cr + 4 * lane);
-        const int4 m4 = *reinterpret_cast<const int4*>(cm + 4 * lane);
-        const float chs[4] = {s4.x, s4.y, s4.z, s4.w};
-        const float chr[4] = {r4.x, r4.y, r4.z, r4.w};
-        const int chm[4] = {m4.x, m4.y, m4.z, m4.w};
+        // pass 2: codes of rows (8a+2g, 8a+2g+1) are bytes 8a+2g, +1 of output row 2c+j
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            uint32_t o4[RQ_ROWS / 4];
-            if (chm[c] == 1) {
-                const float2 r2 = make_float2(chr[c], chr[c]);
-                const float2 ns2 = make_float2(-chs[c], -chs[c]);
+        for (int j = 0; j < 2; ++j) {
+            uint8_t* orow = wst + (2 * c + j) * 128;
+            if (chm[j] == 1) {
+                const float2 r2 = make_float2(chr[j], chr[j]);
+                const float2 ns2 = make_float2(-chs[j], -chs[j]);
 #pragma unroll
-                for (int k = 0; k < RQ_ROWS / 4; ++k) {
-                    const uint32_t c0 =
-                        e4m3_pair(div2_markstein(make_float2(xv[4 * k][c], xv[4 * k + 1][c]), r2, ns2));
-                    const uint32_t c1 =
-                        e4m3_pair(div2_markstein(make_float2(xv[4 * k + 2][c], xv[4 * k + 3][c]), r2, ns2));
-                    // byte c of the four input words: their sign bits are the codes' sign bits
-                    const uint32_t sel = static_cast<uint32_t>(c) | (static_cast<uint32_t>(c + 4) << 4);
-                    const uint32_t in4 = __byte_perm(__byte_perm(wv[4 * k], wv[4 * k + 1], sel),
-                                                     __byte_perm(wv[4 * k + 2], wv[4 * k + 3], sel), 0x5410);
-                    o4[k] = __byte_perm(c0, c1, 0x5410) | (in4 & 0x80808080u);
+                for (int aa = 0; aa < 16; ++aa) {
+                    const uint32_t code = e4m3_pair(div2_markstein(make_float2(xv[aa][j], xv[aa][2 + j]), r2, ns2));
+                    // sign bits of the two dequantized values: bit 7 of their top bytes
+                    const uint32_t top =
+                        __byte_perm(__float_as_uint(xv[aa][j]), __float_as_uint(xv[aa][2 + j]), 0x0073);
+                    sts_u16(orow + (((aa >> 1) ^ c) << 4) + 8 * (aa & 1) + 2 * g, code | (top & 0x8080u));
                 }
             } else {
 #pragma unroll
-                for (int k = 0; k < RQ_ROWS / 4; ++k) {
-                    uint32_t o = 0u;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) o |= quant_div(xv[4 * k + u][c], chs[c], chm[c]) << (8 * u);
-                    o4[k] = o;
+                for (int aa = 0; aa < 16; ++aa) {
+                    const uint32_t code = quant_div(xv[aa][j], chs[j], chm[j]) |
+                                          (quant_div(xv[aa][2 + j], chs[j], chm[j]) << 8);
+                    sts_u16(orow + (((aa >> 1) ^ c) << 4) + 8 * (aa & 1) + 2 * g, code);
                 }
             }
-            sts_v4(out + stage_row<2>(4 * lane + c) + RQ_ROWS * warp, make_uint4(o4[0], o4[1], o4[2], o4[3]));
         }
-        __syncthreads();   // staged tile complete; this stage, red[] and the channel scales are free
-        uint8_t* dst = a.qT + static_cast<int64_t>(kb * 128) * a.ldqT + mb * 128;
+        __syncwarp();
+        uint8_t* dst = a.qT + static_cast<int64_t>(kb * 128 + 16 * w) * a.ldqT + mb * 128;
 #pragma unroll
-        for (int u = 0; u < 1024 / RQ_THREADS; ++u) {
-            const int id = tid + RQ_THREADS * u;    // 128 rows x 8 chunks of 16 bytes
+        for (int u = 0; u < 4; ++u) {
+            const int id = lane + 32 * u;    // 16 rows x 8 chunks of 16 bytes
             const int row = id >> 3, ch = id & 7;
-            stg_v4(dst + static_cast<int64_t>(row) * a.ldqT + 16 * ch, lds_v4(out + stage_row<2>(row) + 16 * ch));
+            stg_v4(dst + static_cast<int64_t>(row) * a.ldqT + 16 * ch, lds_v4(wst + row * 128 + ((ch ^ (row >> 1)) << 4)));
         }
-        const int nxt = blk + RQ_STAGES * gridDim.x;
-        if (nxt < total) issue(stage, nxt);
+        __syncwarp();
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    if (!ok && tid == 0) spin_ns(100000);
+    if (warp == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+    if (!ok && lane == 0) {
+        record_status(kStatusTimeout);
+        spin_ns(100000);   // let the loads still in flight land before the CTA may exit
+    }
 }
 
 }  // namespace fp8fg
