@@ -32,7 +32,10 @@
 //     partial (each warp: its 32 TMEM lanes = rows, one 128-column half, in
 //     four 32-column loads, two in flight), release of the TMEM buffer to the
 //     even CTA as soon as the last two loads land, acc += partial * sA * sB in
-//     FP32 registers with packed FP32x2 FMAs, bf16 stores at tile end.
+//     FP32 registers with packed FP32x2 FMAs, bf16 stores at tile end.  With
+//     per-column B scales (weight gradient) the loads use the 16x128b shape
+//     instead, so that a thread holds one column in four of four rows and
+//     reads 32 column scales per K-block rather than all 128 of its half.
 //   The MMA of K-block kb+1 runs while K-block kb is promoted.
 #pragma once
 
@@ -180,6 +183,24 @@ __device__ __forceinline__ void promote32(float (&acc)[128], const uint32_t (&r)
             acc[OFF + j + 2] = a1.x;
             acc[OFF + j + 3] = a1.y;
         }
+    }
+}
+
+// Column-scale promotion of part of one 16x128b chunk (see
+// tmem_ld_16x128b_x16): the thread's two rows (sa2 = their row scales) at its
+// columns J0 .. J0+NJ-1 of the chunk (one column in four), sb[j - J0] their
+// scales; acc[32 CH + 2j + e] is row e at column j.  Same arithmetic as
+// promote32: acc += partial * (sA sB).
+template <int CH, int J0, int NJ>
+__device__ __forceinline__ void promote_col16(float (&acc)[128], const uint32_t (&r)[32], float2 sa2,
+                                              const float (&sb)[NJ]) {
+#pragma unroll
+    for (int j = J0; j < J0 + NJ; ++j) {
+        const float2 w = __fmul2_rn(sa2, make_float2(sb[j - J0], sb[j - J0]));
+        float2 a = make_float2(acc[32 * CH + 2 * j], acc[32 * CH + 2 * j + 1]);
+        a = __ffma2_rn(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), w, a);
+        acc[32 * CH + 2 * j] = a.x;
+        acc[32 * CH + 2 * j + 1] = a.y;
     }
 }
 
@@ -405,7 +426,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------- promotion and epilogue ----
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
-        const int row = quarter * 32 + lane;    // row of this CTA's 128-row half
+        const int row = quarter * 32 + lane;    // row of this CTA's 128-row half (32x32b loads)
+        const int r4 = lane >> 2, q4 = lane & 3; // 16x128b loads: rows r4 (+8, +16, +24), columns q4 mod 4
         uint32_t it = 0;   // K-blocks promoted so far; every ring position derives from it
         bool ok = true;
         for (int t = pair; ok && t < num_tiles; t += n_pairs) {
@@ -424,24 +446,60 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const float sa = sm_sa[slot * BM + row];
-                const float* sbv = sm_sb + slot * BN + half * 128;
-                const float sc = (SBK == SB_BLOCK) ? __fmul_rn(sa, sm_sb[slot * BN + half]) : 0.0f;
                 const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * BN + half * 128;
                 uint32_t r0[32], r1[32];
-                tmem_ld_32cols(taddr + 0, r0);
-                tmem_ld_32cols(taddr + 32, r1);
-                tmem_wait_ld2(r0, r1);
-                promote32<SBK, 0>(acc, r0, sc, sa, sbv);
-                tmem_ld_32cols(taddr + 64, r0);
-                promote32<SBK, 32>(acc, r1, sc, sa, sbv);
-                tmem_ld_32cols(taddr + 96, r1);
-                tmem_wait_ld2(r0, r1);
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&tempty[buf]), 0));  // the even CTA's
-                promote32<SBK, 64>(acc, r0, sc, sa, sbv);
-                promote32<SBK, 96>(acc, r1, sc, sa, sbv);
+                if constexpr (SBK == SB_COL) {
+                    // 16x128b chunks: ch = (lane half L = 16 (ch & 1), column half C = 64 (ch >> 1));
+                    // a thread needs only the scales of its 32 columns (one column in four),
+                    // each shared by both lane halves and loaded eight at a time
+                    const float* sav = sm_sa + slot * BM + quarter * 32 + r4;
+                    const float2 sa_lo = make_float2(sav[0], sav[8]);
+                    const float2 sa_hi = make_float2(sav[16], sav[24]);
+                    const float* sbw = sm_sb + slot * BN + half * 128 + q4;
+                    float sbv[8];
+                    tmem_ld_16x128b_x16(taddr, r0);
+                    tmem_ld_16x128b_x16(taddr + (16u << 16), r1);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sbv[j] = sbw[4 * j];
+                    tmem_wait_ld2(r0, r1);
+                    promote_col16<0, 0, 8>(acc, r0, sa_lo, sbv);
+                    promote_col16<1, 0, 8>(acc, r1, sa_hi, sbv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sbv[j] = sbw[32 + 4 * j];
+                    promote_col16<0, 8, 8>(acc, r0, sa_lo, sbv);
+                    tmem_ld_16x128b_x16(taddr + 64, r0);
+                    promote_col16<1, 8, 8>(acc, r1, sa_hi, sbv);
+                    tmem_ld_16x128b_x16(taddr + (16u << 16) + 64, r1);
+                    tmem_wait_ld2(r0, r1);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&tempty[buf]), 0));  // the even CTA's
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sbv[j] = sbw[64 + 4 * j];
+                    promote_col16<2, 0, 8>(acc, r0, sa_lo, sbv);
+                    promote_col16<3, 0, 8>(acc, r1, sa_hi, sbv);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) sbv[j] = sbw[96 + 4 * j];
+                    promote_col16<2, 8, 8>(acc, r0, sa_lo, sbv);
+                    promote_col16<3, 8, 8>(acc, r1, sa_hi, sbv);
+                } else {
+                    const float sa = sm_sa[slot * BM + row];
+                    const float* sbv = sm_sb + slot * BN + half * 128;
+                    const float sc = __fmul_rn(sa, sm_sb[slot * BN + half]);
+                    tmem_ld_32cols(taddr + 0, r0);
+                    tmem_ld_32cols(taddr + 32, r1);
+                    tmem_wait_ld2(r0, r1);
+                    promote32<SBK, 0>(acc, r0, sc, sa, sbv);
+                    tmem_ld_32cols(taddr + 64, r0);
+                    promote32<SBK, 32>(acc, r1, sc, sa, sbv);
+                    tmem_ld_32cols(taddr + 96, r1);
+                    tmem_wait_ld2(r0, r1);
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&tempty[buf]), 0));  // the even CTA's
+                    promote32<SBK, 64>(acc, r0, sc, sa, sbv);
+                    promote32<SBK, 96>(acc, r1, sc, sa, sbv);
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sempty[slot]);
             }
@@ -449,6 +507,72 @@ __global__ void __launch_bounds__(THREADS, 1)
             const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
             const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
             const int n0 = tl.nb * BN + half * 128;
+            if constexpr (SBK == SB_COL) {
+                // rows and groups are whole 128-row blocks: the test is uniform per CTA
+                const int g0 = tl.row0 + static_cast<int>(rank) * BM + quarter * 32 + r4;
+                if (!(tl.row0 + static_cast<int>(rank) * BM < tl.row_end && n0 < p.N)) continue;
+#pragma unroll
+                for (int rs = 0; rs < 4; ++rs) {          // rows g0 + 16 (rs >> 1) + 8 (rs & 1)
+                    const int grw = g0 + 16 * (rs >> 1) + 8 * (rs & 1);
+                    const int e = rs & 1, lh = rs >> 1;
+                    if constexpr (QOUT) {
+                        // the row's 128 columns sit in the four lanes of this quad
+                        uint32_t w[16];
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                w[8 * c + k] = pack_bf16x2(acc[32 * (2 * c + lh) + 2 * (2 * k) + e],
+                                                           acc[32 * (2 * c + lh) + 2 * (2 * k + 1) + e]);
+                        uint32_t h = 0u;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) h = umax16x2(h, w[k] & 0x7FFF7FFFu);
+                        h = umax16x2(h, __shfl_xor_sync(0xffffffffu, h, 1));
+                        h = umax16x2(h, __shfl_xor_sync(0xffffffffu, h, 2));
+                        const GroupScale gs = group_scale(hmax_bf16x2_to_f32(h));
+                        uint8_t* qrow = qo.Cq + static_cast<int64_t>(grw) * qo.ldcq + n0 + q4;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int k = 0; k < 2; ++k) {
+                                // codes of columns 64c + 4j + q4, j = 8k .. 8k+7
+                                const uint2 cd = quant8_bf16(
+                                    make_uint4(w[8 * c + 4 * k], w[8 * c + 4 * k + 1], w[8 * c + 4 * k + 2],
+                                               w[8 * c + 4 * k + 3]),
+                                    gs);
+#pragma unroll
+                                for (int b = 0; b < 8; ++b)
+                                    qrow[64 * c + 4 * (8 * k + b)] =
+                                        static_cast<uint8_t>(((b < 4 ? cd.x : cd.y) >> (8 * (b & 3))) & 0xFFu);
+                            }
+                        if (q4 == 0)
+                            qo.sC[static_cast<int64_t>(grw) * qo.sc_m + static_cast<int64_t>(n0 / 128) * qo.sc_nb] =
+                                gs.s;
+                    } else {
+                        // 4x4 transposes of bf16 across the quad, two shuffles each: lane q
+                        // then holds columns 4(4g + q) .. +3 and writes them with one 8-byte store
+                        uint16_t* crow = p.C + static_cast<int64_t>(grw) * p.ldc + n0 + 4 * q4;
+                        const uint32_t sel_w0 = (q4 == 0) ? 0x5410u : (q4 == 1) ? 0x3254u : (q4 == 2) ? 0x7610u : 0x3276u;
+                        const uint32_t sel_w1 = (q4 == 0) ? 0x7610u : (q4 == 1) ? 0x3276u : (q4 == 2) ? 0x5410u : 0x3254u;
+#pragma unroll
+                        for (int c = 0; c < 2; ++c)
+#pragma unroll
+                            for (int g = 0; g < 4; ++g) {
+                                const float* v = acc + 32 * (2 * c + lh) + 8 * g + e;   // v[2k]: column 4(4g+k) + q
+                                const uint32_t p0 = pack_bf16x2(v[0], v[2]);
+                                const uint32_t p1 = pack_bf16x2(v[4], v[6]);
+                                const uint32_t x = (q4 & 2) ? p1 : p0;
+                                const uint32_t y = __shfl_xor_sync(0xffffffffu, (q4 & 2) ? p0 : p1, 2);
+                                const uint32_t rr =
+                                    __shfl_xor_sync(0xffffffffu, __byte_perm(x, y, (q4 & 1) ? 0x5410u : 0x7632u), 1);
+                                const uint32_t a = (q4 & 2) ? y : x;
+                                const uint32_t b = (q4 & 2) ? x : y;
+                                stg_v2(crow + 64 * c + 16 * g, make_uint2(__byte_perm(a, rr, sel_w0), __byte_perm(b, rr, sel_w1)));
+                            }
+                    }
+                }
+                continue;
+            }
             if (!(grow < tl.row_end && n0 < p.N)) continue;
             if constexpr (QOUT) {
                 // bf16 rounding of the output as the plain epilogue does, then the
