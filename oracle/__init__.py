@@ -14,6 +14,9 @@ the plain logical ones:
 * ``quant_w_128x128(w[K,N]) -> (q[K,N], s[K/128,N/128])`` (same figure)
 * ``requant_1x128_to_128x1(q[M,K], s[M,K/128]) -> (qT[K,M], sT[K,M/128])``
   (same page: 1x128 tiles become 128x1 tiles for the backward pass)
+* the three quantizers take ``pow2=True`` for power-of-two scales, the smallest
+  2^e >= amax/448 (why-be.why-be.co.kr post 55081 and sunipension.com post
+  314414: scaling factors that are integral powers of 2)
 * ``gemm_blockscaled(A[M,K], sA[M,K/128], Bt[N,K], sB, sb_kind) -> C[M,N] float64``
   (why-be.why-be.co.kr post 55081, Figure 7(b): FP32 promotion of partials
   per 128-wide K interval, with the two scales applied there)
@@ -50,6 +53,9 @@ def _load():
         lib.orc_quant_act_1x128.argtypes = [vp, i64, i64, i64, vp, i64, vp]
         lib.orc_quant_w_128x128.argtypes = [vp, i64, i64, i64, vp, i64, vp]
         lib.orc_requant_1x128_to_128x1.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
+        lib.orc_quant_act_1x128_pow2.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+        lib.orc_quant_w_128x128_pow2.argtypes = [vp, i64, i64, i64, vp, i64, vp]
+        lib.orc_requant_1x128_to_128x1_pow2.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
         lib.orc_gemm_blockscaled.argtypes = [vp, i64, vp, vp, i64, vp, i32, i64, i64, i64, vp]
         lib.orc_gemm_blockscaled_sample.argtypes = [vp, i64, vp, vp, i64, vp, i32, i64, i64,
                                                     i64, vp, vp, i64, vp]
@@ -58,7 +64,9 @@ def _load():
         lib.orc_grouped_gemm_blockscaled_sample.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64,
                                                             i64, i64, vp, vp, i64, vp]
         for name in ("orc_quant_act_1x128", "orc_quant_w_128x128",
-                     "orc_requant_1x128_to_128x1", "orc_gemm_blockscaled",
+                     "orc_requant_1x128_to_128x1", "orc_quant_act_1x128_pow2",
+                     "orc_quant_w_128x128_pow2", "orc_requant_1x128_to_128x1_pow2",
+                     "orc_gemm_blockscaled",
                      "orc_gemm_blockscaled_sample", "orc_grouped_gemm_blockscaled",
                      "orc_grouped_gemm_blockscaled_sample"):
             getattr(lib, name).restype = ctypes.c_int
@@ -122,43 +130,47 @@ def default_threads():
     return max(1, min(32, os.cpu_count() or 1))
 
 
-def quant_act_1x128(x, threads=None):
+def quant_act_1x128(x, threads=None, pow2=False):
     """x: uint16 bf16 bits [M, K] -> (q uint8 [M, K], s float32 [M, K/128]).
-    `threads` splits the rows (each 1x128 group lies in one row)."""
+    `threads` splits the rows (each 1x128 group lies in one row).  pow2: the
+    power-of-two scale reading (smallest 2^e >= amax/448)."""
     x = _c(x, np.uint16)
     M, K = x.shape
     q = np.empty((M, K), np.uint8)
     s = np.empty((M, K // 128), np.float32)
     lib = _load()
+    fn = lib.orc_quant_act_1x128_pow2 if pow2 else lib.orc_quant_act_1x128
 
     def job(r0, r1):
-        return lambda: _check(lib.orc_quant_act_1x128(_p(x[r0:]), r1 - r0, K, K, _p(q[r0:]), K,
-                                                      _p(s[r0:])), "quant_act_1x128")
+        return lambda: _check(fn(_p(x[r0:]), r1 - r0, K, K, _p(q[r0:]), K, _p(s[r0:])), "quant_act_1x128")
     _run_parallel([job(a, b) for a, b in _chunks(M, threads or 1, 1)] if M else [], threads)
     return q, s
 
 
-def quant_w_128x128(w, threads=None):
+def quant_w_128x128(w, threads=None, pow2=False):
     """w: uint16 bf16 bits [K, N] -> (q uint8 [K, N], s float32 [K/128, N/128]).
-    `threads` splits the K rows on 128-row block boundaries."""
+    `threads` splits the K rows on 128-row block boundaries.  pow2: the
+    power-of-two scale reading."""
     w = _c(w, np.uint16)
     K, N = w.shape
     q = np.empty((K, N), np.uint8)
     s = np.empty((K // 128, N // 128), np.float32)
     lib = _load()
+    fn = lib.orc_quant_w_128x128_pow2 if pow2 else lib.orc_quant_w_128x128
 
     def job(r0, r1):
-        return lambda: _check(lib.orc_quant_w_128x128(_p(w[r0:]), r1 - r0, N, N, _p(q[r0:]), N,
-                                                      _p(s[r0 // 128:])), "quant_w_128x128")
+        return lambda: _check(fn(_p(w[r0:]), r1 - r0, N, N, _p(q[r0:]), N, _p(s[r0 // 128:])),
+                              "quant_w_128x128")
     if K % 128 or N % 128:
         _check(-1, "quant_w_128x128")
     _run_parallel([job(a, b) for a, b in _chunks(K, threads or 1, 128)] if K else [], threads)
     return q, s
 
 
-def requant_1x128_to_128x1(q, s, threads=None):
+def requant_1x128_to_128x1(q, s, threads=None, pow2=False):
     """(q uint8 [M, K], s float32 [M, K/128]) -> (qT uint8 [K, M], sT float32 [K, M/128]).
-    `threads` splits the channels on 128-channel boundaries."""
+    `threads` splits the channels on 128-channel boundaries.  pow2: power-of-two
+    scales for the 128x1 groups."""
     q = _c(q, np.uint8)
     s = _c(s, np.float32)
     M, K = q.shape
@@ -169,10 +181,11 @@ def requant_1x128_to_128x1(q, s, threads=None):
     if M % 128 or K % 128:
         _check(-1, "requant_1x128_to_128x1")
 
+    fn = lib.orc_requant_1x128_to_128x1_pow2 if pow2 else lib.orc_requant_1x128_to_128x1
+
     def job(k0, k1):
         s_part = np.ascontiguousarray(s[:, k0 // 128:k1 // 128])
-        return lambda: _check(lib.orc_requant_1x128_to_128x1(_p(q[:, k0:]), _p(s_part), M, k1 - k0, K,
-                                                             _p(qT[k0:]), M, _p(sT[k0:])),
+        return lambda: _check(fn(_p(q[:, k0:]), _p(s_part), M, k1 - k0, K, _p(qT[k0:]), M, _p(sT[k0:])),
                               "requant_1x128_to_128x1")
     _run_parallel([job(a, b) for a, b in _chunks(K, threads or 1, 128)] if K and M else [], threads)
     return qT, sT

@@ -39,6 +39,14 @@
  *      the GEMM equals the FP64 product of the dequantized operands, summed in
  *      ascending k.
  *   R7 inputs are finite; NaN/Inf are outside the contract.
+ *   R12 the power-of-two variant (the "_pow2" entry points): the scale is the
+ *      smallest power of two s = 2^e with amax / s <= 448 (the exact
+ *      2^ceil(log2(amax/448))), e clamped below at -127, the smallest scale an
+ *      8-bit exponent (UE8M0) can hold; a zero group keeps s = 0.  The quotient
+ *      x / s is then exact (a power-of-two division), and code = E4M3 RNE of it.
+ *      Pages: why-be.why-be.co.kr post 55081 and sunipension.com post 314414
+ *      give these scales as integral powers of 2 for the inputs of the Linear
+ *      after attention and the gradients before the MoE down-projection.
  */
 #include <math.h>
 #include <stdint.h>
@@ -132,11 +140,22 @@ static float bf16_to_f32(uint16_t h)
     return f;
 }
 
+/* Power-of-two scale of a group with largest magnitude amax > 0, reading
+ * R12: the smallest 2^e (e >= -127) with amax <= 448 * 2^e.  Every comparison
+ * is exact in double. */
+static float pow2_scale(float amax)
+{
+    int e = -127;
+    while (ldexp((double)E4M3_MAX, e) < (double)amax)
+        ++e;
+    return (float)ldexp(1.0, e);
+}
+
 /* Quantize one group of n fp32 values (amax -> scale -> codes), [P1], [P4]
- * Figure 7(a), readings R2-R4.  Element i is read at x[i*xs] and its code is
- * written at q[i*qs]. */
+ * Figure 7(a), readings R2-R4, or R12 when pow2 != 0.  Element i is read at
+ * x[i*xs] and its code is written at q[i*qs]. */
 static void quantize_group(const float *x, int64_t n, int64_t xs,
-                           uint8_t *q, int64_t qs, float *s_out)
+                           uint8_t *q, int64_t qs, float *s_out, int pow2)
 {
     float amax = 0.0f, s;
     int64_t i;
@@ -145,11 +164,16 @@ static void quantize_group(const float *x, int64_t n, int64_t xs,
         if (a > amax)
             amax = a;
     }
-    s = amax / E4M3_MAX;
+    if (pow2)
+        s = (amax == 0.0f) ? 0.0f : pow2_scale(amax);
+    else
+        s = amax / E4M3_MAX;
     *s_out = s;
     for (i = 0; i < n; ++i) {
         if (amax == 0.0f)
             q[i * qs] = 0x00;
+        else if (pow2)   /* exact quotient; only values far below E4M3's range can round */
+            q[i * qs] = orc_e4m3_encode((float)((double)x[i * xs] / (double)s));
         else
             q[i * qs] = orc_e4m3_encode(x[i * xs] / s);
     }
@@ -163,8 +187,8 @@ static void quantize_group(const float *x, int64_t n, int64_t xs,
  *   q  codes [M][K], row stride ldq
  *   s  scales [M][K/128], row-major, dense
  * Returns 0, or -1 when K is not a multiple of 128. */
-int orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
-                        uint8_t *q, int64_t ldq, float *s)
+static int quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                           uint8_t *q, int64_t ldq, float *s, int pow2)
 {
     float buf[Q_GROUP];
     int64_t m, kb, i, KB;
@@ -176,9 +200,22 @@ int orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
             for (i = 0; i < Q_GROUP; ++i)
                 buf[i] = bf16_to_f32(x[m * ldx + kb * Q_GROUP + i]);
             quantize_group(buf, Q_GROUP, 1, q + m * ldq + kb * Q_GROUP, 1,
-                           s + m * KB + kb);
+                           s + m * KB + kb, pow2);
         }
     return 0;
+}
+
+int orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                        uint8_t *q, int64_t ldq, float *s)
+{
+    return quant_act_1x128(x, M, K, ldx, q, ldq, s, 0);
+}
+
+/* The same with power-of-two scales (R12). */
+int orc_quant_act_1x128_pow2(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t *q, int64_t ldq, float *s)
+{
+    return quant_act_1x128(x, M, K, ldx, q, ldq, s, 1);
 }
 
 /* 128x128 weight quantization, [P4] Figure 7(a): W[K][N] (K = input channels,
@@ -187,8 +224,8 @@ int orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
  *   q  codes [K][N] (same layout as w), row stride ldq
  *   s  scales [K/128][N/128], row-major, dense
  * Returns 0, or -1 when K or N is not a multiple of 128. */
-int orc_quant_w_128x128(const uint16_t *w, int64_t K, int64_t N, int64_t ldw,
-                        uint8_t *q, int64_t ldq, float *s)
+static int quant_w_128x128(const uint16_t *w, int64_t K, int64_t N, int64_t ldw,
+                           uint8_t *q, int64_t ldq, float *s, int pow2)
 {
     float blk[Q_GROUP * Q_GROUP];
     uint8_t qb[Q_GROUP * Q_GROUP];
@@ -203,12 +240,25 @@ int orc_quant_w_128x128(const uint16_t *w, int64_t K, int64_t N, int64_t ldw,
                 for (j = 0; j < Q_GROUP; ++j)
                     blk[i * Q_GROUP + j] =
                         bf16_to_f32(w[(kb * Q_GROUP + i) * ldw + nb * Q_GROUP + j]);
-            quantize_group(blk, Q_GROUP * Q_GROUP, 1, qb, 1, s + kb * NB + nb);
+            quantize_group(blk, Q_GROUP * Q_GROUP, 1, qb, 1, s + kb * NB + nb, pow2);
             for (i = 0; i < Q_GROUP; ++i)
                 for (j = 0; j < Q_GROUP; ++j)
                     q[(kb * Q_GROUP + i) * ldq + nb * Q_GROUP + j] = qb[i * Q_GROUP + j];
         }
     return 0;
+}
+
+int orc_quant_w_128x128(const uint16_t *w, int64_t K, int64_t N, int64_t ldw,
+                        uint8_t *q, int64_t ldq, float *s)
+{
+    return quant_w_128x128(w, K, N, ldw, q, ldq, s, 0);
+}
+
+/* The same with power-of-two scales (R12). */
+int orc_quant_w_128x128_pow2(const uint16_t *w, int64_t K, int64_t N, int64_t ldw,
+                             uint8_t *q, int64_t ldq, float *s)
+{
+    return quant_w_128x128(w, K, N, ldw, q, ldq, s, 1);
 }
 
 /* 1x128 -> 128x1 requantization for the backward pass, [P4] ("converted from a
@@ -218,8 +268,8 @@ int orc_quant_w_128x128(const uint16_t *w, int64_t K, int64_t N, int64_t ldw,
  *   q   codes [M][K], row stride ldq;  s  scales [M][K/128] row-major dense
  *   qT  codes [K][M], row stride ldqT; sT scales [K][M/128] row-major dense
  * Returns 0, or -1 when M or K is not a multiple of 128. */
-int orc_requant_1x128_to_128x1(const uint8_t *q, const float *s, int64_t M, int64_t K,
-                               int64_t ldq, uint8_t *qT, int64_t ldqT, float *sT)
+static int requant_1x128_to_128x1(const uint8_t *q, const float *s, int64_t M, int64_t K,
+                                  int64_t ldq, uint8_t *qT, int64_t ldqT, float *sT, int pow2)
 {
     float col[Q_GROUP];
     int64_t k, mb, i, KB, MB;
@@ -235,9 +285,24 @@ int orc_requant_1x128_to_128x1(const uint8_t *q, const float *s, int64_t M, int6
                 col[i] = dec * s[m * KB + k / Q_GROUP];     /* one fp32 multiply */
             }
             quantize_group(col, Q_GROUP, 1, qT + k * ldqT + mb * Q_GROUP, 1,
-                           sT + k * MB + mb);
+                           sT + k * MB + mb, pow2);
         }
     return 0;
+}
+
+int orc_requant_1x128_to_128x1(const uint8_t *q, const float *s, int64_t M, int64_t K,
+                               int64_t ldq, uint8_t *qT, int64_t ldqT, float *sT)
+{
+    return requant_1x128_to_128x1(q, s, M, K, ldq, qT, ldqT, sT, 0);
+}
+
+/* The same with power-of-two scales (R12) for the 128x1 groups; the input
+ * scales are whatever the 1x128 codes were made with (powers of two in the
+ * power-of-two pipeline, so the dequantizing multiply is exact there). */
+int orc_requant_1x128_to_128x1_pow2(const uint8_t *q, const float *s, int64_t M, int64_t K,
+                                    int64_t ldq, uint8_t *qT, int64_t ldqT, float *sT)
+{
+    return requant_1x128_to_128x1(q, s, M, K, ldq, qT, ldqT, sT, 1);
 }
 
 /* ------------------------------------------------------------- GEMMs --- */

@@ -126,3 +126,29 @@ def dequant_f32(code: int, s: np.float32) -> np.float32:
     if sign:
         v = -v
     return np.float32(v)
+
+
+def pow2_scale(amax: Fraction) -> Fraction:
+    """The power-of-two scale of a group (reading R12): the smallest 2^e with
+    amax <= 448 * 2^e, e >= -127; 0 for an all-zero group."""
+    if amax == 0:
+        return Fraction(0)
+    e = -127
+    while E4M3_MAX * Fraction(2) ** e < amax:
+        e += 1
+    return Fraction(2) ** e
+
+
+def quant_group_pow2(values_f32):
+    """Exact reference of one group with a power-of-two scale: s = pow2_scale(amax),
+    code = E4M3(RN32(x / s)).  Returns (scale as float32, list of codes)."""
+    vals = [float_to_fraction(v) for v in np.asarray(values_f32, np.float32).ravel()]
+    amax = max((mag for _, mag in vals), default=Fraction(0))
+    s = pow2_scale(amax)
+    codes = []
+    for sign, mag in vals:
+        if amax == 0:
+            codes.append(0)
+            continue
+        codes.append(e4m3_code_of(sign, e4m3_round(f32_round(mag / s))))
+    return np.float32(float(s)), codes
