@@ -14,6 +14,9 @@ the plain logical ones:
 * ``quant_w_128x128(w[K,N]) -> (q[K,N], s[K/128,N/128])`` (same figure)
 * ``requant_1x128_to_128x1(q[M,K], s[M,K/128]) -> (qT[K,M], sT[K,M/128])``
   (same page: 1x128 tiles become 128x1 tiles for the backward pass)
+* ``swiglu_bf16(gate[M,F], up[M,F]) -> y[M,F]`` bf16 bits of
+  g*u/(1+exp(-g)) in FP64, rounded once (why-be.why-be.co.kr post 65900: the
+  SwiGLU output is recomputed from its cached inputs)
 * the three quantizers take ``pow2=True`` for power-of-two scales, the smallest
   2^e >= amax/448 (why-be.why-be.co.kr post 55081 and sunipension.com post
   314414: scaling factors that are integral powers of 2)
@@ -57,6 +60,8 @@ def _load():
         lib.orc_quant_w_128x128_pow2.argtypes = [vp, i64, i64, i64, vp, i64, vp]
         lib.orc_requant_1x128_to_128x1_pow2.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp]
         lib.orc_gemm_blockscaled.argtypes = [vp, i64, vp, vp, i64, vp, i32, i64, i64, i64, vp]
+        lib.orc_swiglu_bf16.argtypes = [vp, i64, vp, i64, i64, i64, vp, i64]
+        lib.orc_swiglu_bf16.restype = ctypes.c_int64
         lib.orc_gemm_blockscaled_sample.argtypes = [vp, i64, vp, vp, i64, vp, i32, i64, i64,
                                                     i64, vp, vp, i64, vp]
         lib.orc_grouped_gemm_blockscaled.argtypes = [vp, i64, vp, vp, vp, vp, i32, i64, i64,
@@ -257,3 +262,20 @@ def grouped_gemm_blockscaled_sample(A, sA, B, sB, offsets, ms, ns, threads=None)
                               "grouped_gemm_blockscaled_sample")
     _run_parallel([job(a, b) for a, b in _chunks(ms.size, threads or 1, 1)] if ms.size else [], threads)
     return out
+
+
+def swiglu_bf16(gate, up, threads=None):
+    """gate, up: uint16 bf16 bits [M, F] -> y uint16 bf16 bits [M, F],
+    y = bf16(g * u / (1 + exp(-g))) evaluated in FP64 and rounded once."""
+    gate, up = _c(gate, np.uint16), _c(up, np.uint16)
+    assert gate.shape == up.shape
+    M, F = gate.shape
+    y = np.empty((M, F), np.uint16)
+    lib = _load()
+
+    def job(r0, r1):
+        return lambda: lib.orc_swiglu_bf16(_p(gate[r0:]), F, _p(up[r0:]), F, r1 - r0, F, _p(y[r0:]), F)
+    undecided = sum(_run_parallel([job(a, b) for a, b in _chunks(M, threads or 1, 1)] if M else [], threads))
+    if undecided:
+        raise ValueError("oracle swiglu_bf16: %d roundings could not be decided" % undecided)
+    return y

@@ -39,6 +39,12 @@
  *      the GEMM equals the FP64 product of the dequantized operands, summed in
  *      ascending k.
  *   R7 inputs are finite; NaN/Inf are outside the contract.
+ *   R13 SwiGLU recompute: the SwiGLU output y = silu(g) * u = g * u / (1 + e^-g)
+ *      of a cached bf16 gate g and up projection u, evaluated in FP64 (libm
+ *      exp) and rounded once to bf16 (nearest, ties to even), is what the fused
+ *      recompute-and-quantize step 1x128-quantizes.  Page: why-be.why-be.co.kr
+ *      post 65900 (the inputs of the SwiGLU operator are cached and its output
+ *      recomputed in the backward pass).
  *   R12 the power-of-two variant (the "_pow2" entry points): the scale is the
  *      smallest power of two s = 2^e with amax / s <= 448 (the exact
  *      2^ceil(log2(amax/448))), e clamped below at -127, the smallest scale an
@@ -432,4 +438,95 @@ int orc_grouped_gemm_blockscaled_sample(const uint8_t *A, int64_t lda, const flo
                                         ms[i], ns[i], N, K);
     }
     return 0;
+}
+
+/* --------------------------------------------------------------- SwiGLU --- */
+
+/* Round a finite double to the nearest bf16 value, ties to even; bf16 has 8
+ * significant bits, subnormals down to 2^-133, and overflows to infinity
+ * above its largest finite value (2 - 2^-7) * 2^127 by half an ulp or more.
+ * Returns the bf16 bit pattern. */
+static uint16_t bf16_round_double(double v)
+{
+    double a = fabs(v), q, r;
+    int e;
+    uint16_t sign = signbit(v) ? 0x8000 : 0x0000;
+    uint32_t u;
+    float f;
+    if (a == 0.0)
+        return sign;
+    frexp(a, &e);                   /* a = f * 2^e, f in [0.5, 1) */
+    if (e - 1 < -126)
+        e = -125;                   /* subnormal range: quantum 2^-133 */
+    q = ldexp(1.0, e - 8);          /* 8 significant bits: ulp of a */
+    r = nearbyint(a / q) * q;       /* exact scaling by a power of two; nearbyint rounds half to even */
+    if (r >= ldexp(1.0, 128))
+        return (uint16_t)(sign | 0x7F80);
+    f = (float)r;                   /* exact: r has at most 8 significant bits */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (u >> 16));
+}
+
+/* One SwiGLU output, reading R13: bf16 of y = g * u * sigma(g), sigma(g) =
+ * 1 / (1 + e^-g), rounded once to nearest, ties to even.  y is never exactly
+ * a bf16 midpoint (for g != 0, sigma(g) is transcendental), so the rounding
+ * direction is always defined; the value is computed in double, and when it
+ * lies within 2^-45 (relative) of a midpoint m the side is decided again in
+ * long double from quantities free of cancellation:
+ *   g >= 0:  |y| = |gu| - |gu| t with t = 1 / (1 + e^g), so |y| > m exactly
+ *            when |gu| - m (exact) > |gu| t;
+ *   g <  0:  |y| = |gu| e^g / (1 + e^g), compared with m directly.
+ * *ambiguous is set if even that cannot separate |y| from m. */
+static uint16_t swiglu_bf16_one(uint16_t gb, uint16_t ub, int *ambiguous)
+{
+    double g = (double)bf16_to_f32(gb), u = (double)bf16_to_f32(ub);
+    double gu = g * u;              /* exact: at most 16 significant bits */
+    double a, q, lo, mid;
+    int e, above;
+    uint16_t sign, r;
+    if (gu == 0.0)
+        return bf16_round_double(gu);
+    sign = signbit(gu) ? 0x8000 : 0x0000;
+    a = fabs(gu) / (1.0 + exp(-g));
+    frexp(a, &e);
+    if (e - 1 < -126)
+        e = -125;
+    q = ldexp(1.0, e - 8);          /* bf16 quantum at a */
+    lo = floor(a / q) * q;
+    mid = lo + 0.5 * q;
+    if (fabs(a - mid) > ldexp(a, -45))
+        return bf16_round_double(sign ? -a : a);
+    if (g >= 0.0) {
+        long double d = (long double)fabs(gu) - (long double)mid;
+        long double p = (long double)fabs(gu) / (1.0L + expl((long double)g));
+        above = d > p;
+        if (fabsl(d - p) <= ldexpl(p, -58) && p > 0.0L)
+            *ambiguous = 1;
+    } else {
+        long double el = expl((long double)g);
+        long double al = (long double)fabs(gu) * el / (1.0L + el);
+        above = al > (long double)mid;
+        if (fabsl(al - (long double)mid) <= ldexpl(al, -58))
+            *ambiguous = 1;
+    }
+    r = bf16_round_double(above ? lo + q : lo);
+    return (uint16_t)(sign | r);
+}
+
+/* SwiGLU output of cached bf16 inputs, reading R13: for m < M, f < F,
+ * y[m][f] = bf16(g * u / (1 + exp(-g))) with g = gate[m*ldg + f] and
+ * u = up[m*ldu + f], correctly rounded.  y is written as bf16 bit patterns at
+ * y[m*ldy + f].  Returns the number of elements whose rounding direction could
+ * not be decided (expected 0; see swiglu_bf16_one). */
+int64_t orc_swiglu_bf16(const uint16_t *gate, int64_t ldg, const uint16_t *up, int64_t ldu,
+                        int64_t M, int64_t F, uint16_t *y, int64_t ldy)
+{
+    int64_t m, f, undecided = 0;
+    for (m = 0; m < M; ++m)
+        for (f = 0; f < F; ++f) {
+            int amb = 0;
+            y[m * ldy + f] = swiglu_bf16_one(gate[m * ldg + f], up[m * ldu + f], &amb);
+            undecided += amb;
+        }
+    return undecided;
 }

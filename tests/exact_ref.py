@@ -152,3 +152,49 @@ def quant_group_pow2(values_f32):
             continue
         codes.append(e4m3_code_of(sign, e4m3_round(f32_round(mag / s))))
     return np.float32(float(s)), codes
+
+
+def bf16_round(mag: Fraction) -> Fraction:
+    """Round a non-negative exact value to bf16 (8 significant bits),
+    nearest-even, subnormals (quantum 2^-133) kept."""
+    if mag == 0:
+        return Fraction(0)
+    e = max(_exponent(mag), -126)
+    ulp = Fraction(2) ** (e - 7)
+    out = _round_half_even(mag / ulp) * ulp
+    assert out < Fraction(2) ** 128, "overflow is outside the contract"
+    return out
+
+
+def bf16_bits_of(sign: int, mag: Fraction) -> int:
+    """Bit pattern of a bf16 value given exactly (mag must be representable)."""
+    if mag == 0:
+        return sign << 15
+    f = np.float32(float(mag))
+    assert Fraction(float(f)) == mag
+    return (sign << 15) | (int(f.view(np.uint32)) >> 16)
+
+
+def swiglu_bf16_exact(g_bits: int, u_bits: int, digits: int = 60) -> int:
+    """bf16 bits of y = g * u * sigma(g), sigma(g) = 1 / (1 + e^-g), rounded
+    once.  The sigmoid factor is evaluated with `digits` significant decimal
+    digits (decimal's exp is correctly rounded at that precision) in a form
+    that keeps its relative precision for any g: for g >= 0, y = g u (1 - t)
+    with t = 1 / (1 + e^g); for g < 0, y = g u e^g / (1 + e^g).  The rest is
+    exact rational arithmetic."""
+    import decimal
+    ctx = decimal.Context(prec=digits, Emin=-10 ** 9, Emax=10 ** 9)
+    sg, mg = f32_bits_to_fraction(int(g_bits) << 16)
+    su, mu = f32_bits_to_fraction(int(u_bits) << 16)
+    prod = mg * mu
+    sign = sg ^ su
+    if prod == 0:
+        return sign << 15
+    gd = ctx.divide(decimal.Decimal(mg.numerator), decimal.Decimal(mg.denominator))   # |g|
+    e = ctx.exp(gd)                                  # e^|g|
+    t = Fraction(ctx.divide(decimal.Decimal(1), ctx.add(decimal.Decimal(1), e)))     # 1 / (1 + e^|g|)
+    if sg == 0:
+        y = prod * (1 - t)                           # g >= 0: sigma(g) = 1 - 1/(1 + e^g)
+    else:
+        y = prod * t                                 # g < 0: sigma(g) = 1/(1 + e^|g|)
+    return bf16_bits_of(sign, bf16_round(y))
