@@ -10,8 +10,9 @@ FP8 training step of a large MoE transformer layer:
   data gradient of that layer         dY bf16 [8192, 18432] -> 1x128 quantize;
                                       W -> 128x128 quantize (row-major codes);
                                       dX = GEMM (1x128 x 128x128 scales) bf16 [8192, 7168]
-  weight gradient of that layer       (dY quantized above)
-                                      cached Xq and dYq -> 1x128 -> 128x1 requantize;
+  weight gradient of that layer       Xw bf16 [8192, 7168] ~ N(0, 1e-3^2) with 0.1% elements
+                                      x1000 -> 1x128 quantize (dY quantized above);
+                                      cached Xwq and dYq -> 1x128 -> 128x1 requantize;
                                       dW = GEMM (128x1 x 128x1 scales) bf16 [7168, 18432]
   MoE expert forward                  16384 tokens x 8 picks (Zipf 1.1 over 32 experts,
                                       padded to 128 rows) bf16 [~133k, 7168] -> 1x128 quantize;
@@ -68,6 +69,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    p.add_argument("--steady-seconds", type=float, default=2.0,
+                   help="length of the steady-state leg (clock record under sustained load; 0 skips it)")
     return p.parse_args()
 
 
@@ -81,6 +84,7 @@ class Workload:
         self.x, _ = synth.activation(2 + s, T, CIN)                     # 1% channels x100
         self.w = synth.weight(2 + s, CIN, COUT)                         # N(0, 0.02^2)
         self.dy = synth.wgrad_tensor(4 + s, 1, T, COUT)                 # N(0,1e-3^2), 0.1% x1000
+        self.xw = synth.wgrad_tensor(4 + s, 0, T, CIN)                  # the weight gradient's X, same recipe
         moe = synth.moe_inputs(seed=5 + s, G=G, K=MOE_K, N=MOE_N, tokens=TOKENS, topk=TOPK, zipf_s=ZIPF)
         self.moe_x = moe.x
         self.moe_w = moe.w
@@ -108,6 +112,7 @@ class Workload:
             "quant_w": q(CIN, COUT) - CIN * COUT // 128 * 4 + (CIN // 128) * (COUT // 128) * 4,
             "quant_w_rowmajor": q(CIN, COUT) - CIN * COUT // 128 * 4 + (CIN // 128) * (COUT // 128) * 4,
             "quant_act_dy": q(T, COUT),
+            "quant_act_xw": q(T, CIN),
             "requant_x": rq(T, CIN),
             "requant_dy": rq(T, COUT),
             "quant_act_moe": q(self.moe_rows, MOE_K),
@@ -129,6 +134,8 @@ class Workload:
                           "[7168x18432] (K-major and row-major codes), 32x[7168x2048]; "
                           "1x128->128x1 requant of [8192x7168], "
                           "[8192x18432]" % self.moe_rows,
+            "wgrad_inputs": "X [8192x7168] and dY [8192x18432] ~ N(0, 1e-3^2) with Bernoulli(0.001) "
+                            "elements x1000, each 1x128-quantized then requantized 128x1 along tokens",
             "l2": "inputs larger than L2 (126 MB); %.1f GB of quantizer traffic per step"
                   % (sum(self.quant_bytes().values()) / 1e9),
             "global_batch": T,
@@ -142,8 +149,9 @@ class DeviceStep:
     """Device buffers and the sequence of library calls of one step."""
 
     KERNELS = ["quant_act_x", "quant_w", "gemm_fprop", "quant_act_dy", "quant_w_rowmajor", "gemm_dgrad",
-               "requant_x", "requant_dy", "gemm_wgrad", "quant_act_moe", "quant_w_moe", "grouped_gemm_moe"]
-    LAUNCHES_PER_STEP = 12      # the 32 expert weights are quantized in one batched launch
+               "quant_act_xw", "requant_x", "requant_dy", "gemm_wgrad", "quant_act_moe", "quant_w_moe",
+               "grouped_gemm_moe"]
+    LAUNCHES_PER_STEP = 13      # the 32 expert weights are quantized in one batched launch
 
     def __init__(self, wl, device):
         import torch
@@ -160,6 +168,7 @@ class DeviceStep:
         self.x = e((T, CIN), bf)
         self.w = e((CIN, COUT), bf)
         self.dy = e((T, COUT), bf)
+        self.xw = e((T, CIN), bf)
         self.moe_x = e((wl.moe_rows, MOE_K), bf)
         self.moe_w = e((G, MOE_K, MOE_N), bf)
         self.moe_off = e((G + 1,), torch.int32)
@@ -168,6 +177,7 @@ class DeviceStep:
         self.wq, self.sw = e((COUT, CIN), u8), e((CIN // 128, COUT // 128), f32)
         self.wq_rm, self.sw_rm = e((CIN, COUT), u8), e((CIN // 128, COUT // 128), f32)
         self.dyq, self.sdy = e((T, COUT), u8), e((COUT // 128, T), f32).t()
+        self.xwq, self.sxw = e((T, CIN), u8), e((CIN // 128, T), f32).t()
         self.xqT, self.sxT = e((CIN, T), u8), e((T // 128, CIN), f32).t()
         self.dyqT, self.sdyT = e((COUT, T), u8), e((T // 128, COUT), f32).t()
         self.mxq, self.smx = e((wl.moe_rows, MOE_K), u8), e((MOE_K // 128, wl.moe_rows), f32).t()
@@ -187,6 +197,7 @@ class DeviceStep:
         self.x.copy_(bf16(wl.x))
         self.w.copy_(bf16(wl.w))
         self.dy.copy_(bf16(wl.dy))
+        self.xw.copy_(bf16(wl.xw))
         self.moe_x.copy_(bf16(wl.moe_x))
         self.moe_w.copy_(bf16(wl.moe_w))
         self.moe_off.copy_(torch.from_numpy(wl.moe_offsets))
@@ -221,8 +232,11 @@ class DeviceStep:
         fg.fp8_gemm_blockscaled(self.dyq, self.sdy, self.wq_rm, self.sw_rm.t(), fg.FP8_SB_BLOCK128x128, self.dx,
                                 stream=stream)
         rec("gemm_dgrad", 1)
+        rec("quant_act_xw", 0)
+        fg.fp8_quant_act_1x128(self.xw, self.xwq, self.sxw, stream=stream)
+        rec("quant_act_xw", 1)
         rec("requant_x", 0)
-        fg.fp8_requant_1x128_to_128x1(self.xq, self.sx, self.xqT, self.sxT, stream=stream)
+        fg.fp8_requant_1x128_to_128x1(self.xwq, self.sxw, self.xqT, self.sxT, stream=stream)
         rec("requant_x", 1)
         rec("requant_dy", 0)
         fg.fp8_requant_1x128_to_128x1(self.dyq, self.sdy, self.dyqT, self.sdyT, stream=stream)
@@ -255,6 +269,39 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# Dense FP8 tensor-core rate per clock of the whole chip: 148 SMs x 8192 FP8
+# multiply-adds per SM per clock x 2 flops (4.93 PFLOP/s at the 2032 MHz
+# maximum SM clock).  Used only for the clock-scaled context fraction.
+NOMINAL_FP8_FLOP_PER_CLK = 148 * 8192 * 2
+
+
+def choose_fp8_peak(ms_total, clk, burst, sustained):
+    """The FP8 roofline denominator: the burst figure (cuBLAS bf16 timed alone,
+    x2) for a timed region shorter than one second or one whose median SM
+    clock stayed within 5% of the maximum; the sustained figure (a seconds-long
+    bf16 loop under the power cap, x2) otherwise.  Returns (peak, rule)."""
+    sm, smax = clk.get("sm_mhz"), clk.get("sm_max_mhz")
+    if ms_total < 1000.0:
+        return burst, "burst: timed region %.2f s < 1 s" % (ms_total / 1e3)
+    if sm and smax and sm >= 0.95 * smax:
+        return burst, "burst: median SM clock %.0f MHz within 5%% of %.0f" % (sm, smax)
+    return sustained, "sustained: timed region %.2f s, median SM clock %s MHz" % (ms_total / 1e3, sm)
+
+
+def load_tensor_pipe():
+    """ncu tensor-pipe activity (% of cycles) of each GEMM from the committed
+    profile summary, valid only while the kernel sources are unchanged."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return {}
+    if t.get("source_hash") != kernel_source_hash():
+        return {}
+    return t.get("tensor_pipe_active_pct", {})
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in ("ptx.cuh", "quant.cuh", "gemm.cuh", "fp8fg.cu"):
@@ -278,8 +325,10 @@ def load_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle-reason samples (every 50 ms) while the timed
+    region runs; only samples whose timestamps fall inside the window given to
+    stop() are kept."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -292,12 +341,24 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
+
+    def stop(self, t0=None, t1=None):
+        """Summary of the samples taken between wall-clock times t0 and t1
+        (all samples if none falls inside)."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -306,30 +367,34 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, power, reasons = [], [], [], set()
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                    power.append(float(parts[3]))
+                    rows.append((self._when(parts[0]), float(parts[2]), float(parts[3]), float(parts[4]),
+                                 {n for n, v in zip(names, parts[6:10]) if v.lower().startswith("active")}))
                 except ValueError:
                     continue
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower().startswith("active"):
-                        reasons.add(name)
         try:
             os.remove(self.path)
         except OSError:
             pass
+        inside = [r for r in rows if t0 is not None and r[0] is not None and t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "whole sampling period (no sample inside the timed region)"
+        sm = [r[1] for r in inside]
+        reasons = set()
+        for r in inside:
+            reasons |= r[4]
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_median": statistics.median(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+                "power_w_median": statistics.median(r[3] for r in inside) if inside else None,
+                "samples": len(inside), "window": window, "interval_ms": 50, "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------- CPU oracle leg ----
@@ -358,7 +423,8 @@ def cpu_oracle_sample(wl, frac, threads=1):
         return out, time.perf_counter() - t0
 
     # 1x128 activation quantization: whole rows
-    act_elems = {"x": (wl.x, T * CIN), "dy": (wl.dy, T * COUT), "moe": (wl.moe_x, wl.moe_rows * MOE_K)}
+    act_elems = {"x": (wl.x, T * CIN), "dy": (wl.dy, T * COUT), "xw": (wl.xw, T * CIN),
+                 "moe": (wl.moe_x, wl.moe_rows * MOE_K)}
     est = 0.0
     for name, (arr, n_full) in act_elems.items():
         rows = max(1, int(round(frac * arr.shape[0])))
@@ -376,7 +442,7 @@ def cpu_oracle_sample(wl, frac, threads=1):
         est += dt * n_full / (128 * cols)
         parts.append("weight %s 128x%d" % (name, cols))
     # requantization: one 128-token block x a fraction of the channels
-    for name, arr, n_full in (("x", wl.x, T * CIN), ("dy", wl.dy, T * COUT)):
+    for name, arr, n_full in (("x", wl.xw, T * CIN), ("dy", wl.dy, T * COUT)):
         q, s = oracle.quant_act_1x128(arr[:128])
         cols = min(arr.shape[1], max(128, int(round(frac * arr.size / 128)) // 128 * 128))
         _, dt = timed(lambda: oracle.requant_1x128_to_128x1(np.ascontiguousarray(q[:, :cols]),
@@ -471,12 +537,14 @@ def run_reference(args, world, rank):
     value = flops / est_step / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": est_step * 1e3,
-        "sample_ms_per_step": statistics.mean(samples) * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(samples) * 1e3,
+        "extrapolated_ms_per_full_step": est_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": wl.describe(),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": "fraction %.3g of each kernel's work per step: %s" % (frac, desc)},
+                         "sample": "fraction %.3g of each kernel's work per step: %s; ms_per_step is the "
+                                   "measured time of that sample, value the step's GEMM work over the "
+                                   "sample time scaled to the whole step" % (frac, desc)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -529,13 +597,15 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    wall0 = time.time()
     with torch.cuda.stream(stream):
         t0.record(stream)
         for i in range(args.steps):
             step.run(stream, evs[i])
         t1.record(stream)
     torch.cuda.synchronize()
-    clk = clocks.stop()
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
     if world > 1:
         dist.barrier()
     ms_total = max_over_ranks(t0.elapsed_time(t1), world, device)
@@ -546,16 +616,27 @@ def main():
     per_kernel_ms = {k: statistics.mean(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(args.steps))
                      for k in DeviceStep.KERNELS}
     peaks, peak_src = load_peaks()
-    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    fp8_peak_sustained = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
     fp8_peak_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
+    fp8_peak, peak_rule = choose_fp8_peak(ms_total, clk, fp8_peak_burst, fp8_peak_sustained)
+    sm_mhz = clk.get("sm_mhz")
+    fp8_nominal = NOMINAL_FP8_FLOP_PER_CLK * sm_mhz * 1e6 / 1e12 if sm_mhz else None
     hbm = peaks["hbm_gbs"]
     traffic = load_traffic()
+    pipes = load_tensor_pipe()
     kernels = {}
     for k, ms in per_kernel_ms.items():
         d = {"ms": ms, "launches_per_step": 1}
+        if sm_mhz:
+            d["kcycles_at_median_clock"] = ms * sm_mhz
         if k in flops:
             tf = flops[k] / (ms * 1e-3) / 1e12
-            d.update({"tflops": tf, "frac_fp8_sustained": tf / fp8_peak, "frac_fp8_burst": tf / fp8_peak_burst})
+            d.update({"tflops": tf, "frac_fp8": tf / fp8_peak, "frac_fp8_burst": tf / fp8_peak_burst,
+                      "frac_fp8_sustained": tf / fp8_peak_sustained})
+            if fp8_nominal:
+                d["frac_fp8_nominal_at_clock"] = tf / fp8_nominal
+            if k in pipes:
+                d["ncu_tensor_pipe_active"] = pipes[k]
         else:
             gbs = qbytes[k] / (ms * 1e-3) / 1e9
             d.update({"gbs": gbs, "frac_hbm": gbs / hbm, "bytes": qbytes[k]})
@@ -565,14 +646,22 @@ def main():
         ach = flops[dom] / (per_kernel_ms[dom] * 1e-3) / 1e12
         roofline = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s",
                     "frac": ach / fp8_peak, "traffic": traffic.get(dom),
-                    "peak_source": "%s sustained bf16 x %.0f (nominal FP8/BF16 ratio)" % (peak_src, FP8_OVER_BF16)}
+                    "peak_source": "%s bf16 x %.0f (nominal FP8/BF16 ratio), %s" % (peak_src, FP8_OVER_BF16,
+                                                                                   peak_rule),
+                    "frac_nominal_at_clock": (ach / fp8_nominal) if fp8_nominal else None,
+                    "frac_tensor_pipe": pipes.get(dom)}
     else:
-        launches = kernels[dom]["launches_per_step"]
         ach = qbytes[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
                     "frac": ach / hbm, "traffic": traffic.get(dom), "peak_source": peak_src + " copy"}
     if roofline["traffic"] is not None:
         roofline["traffic"] = float(roofline["traffic"])
+
+    # steady state: the same step back to back for a few seconds, with tens of
+    # clock samples (context for the short timed region above)
+    steady = None
+    if args.steady_seconds > 0:
+        steady = run_steady(args, step, stream, smi_id(torch, local), ms_step, world)
 
     # end-to-end: pinned host inputs -> device -> step -> outputs back to pinned host
     e2e = None
@@ -596,15 +685,45 @@ def main():
             "roofline": roofline, "kernels": kernels,
             "quantizers_gbs": sum(qbytes.values()) / (sum(per_kernel_ms[k] for k in qbytes) * 1e-3) / 1e9,
             "gemms_tflops": total_flops / (sum(per_kernel_ms[k] for k in flops) * 1e-3) / 1e12,
-            "fp8_peak_tflops": {"sustained": fp8_peak, "burst": fp8_peak_burst, "source": peak_src},
+            "fp8_peak_tflops": {"used": fp8_peak, "rule": peak_rule, "sustained": fp8_peak_sustained,
+                                "burst": fp8_peak_burst, "nominal_at_median_clock": fp8_nominal,
+                                "source": peak_src},
             "hbm_peak_gbs": hbm,
-            "cpu_baseline": cpu, "e2e": e2e,
+            "cpu_baseline": cpu, "e2e": e2e, "steady_state": steady,
             "gpu_launches": DeviceStep.LAUNCHES_PER_STEP * args.steps,
             "clocks": clk, "device_status": status,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_steady(args, step, stream, gpu, ms_step, world):
+    """Run the step back to back for about args.steady_seconds with an event
+    pair around every step, sampling clocks every 50 ms.  Returns the median
+    step time, the clock record and step times grouped by the SM clock of the
+    nearest sample (100 MHz bins)."""
+    import torch
+    n = max(10, int(args.steady_seconds * 1e3 / max(ms_step, 1e-3)))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    clocks = ClockSampler(gpu)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            evs[i][0].record(stream)
+            step.run(stream)
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return {"steps": n, "seconds": wall1 - wall0, "ms_per_step_median": statistics.median(ms),
+            "ms_per_step_min": min(ms), "ms_per_step_last_quarter": statistics.median(ms[3 * n // 4:]),
+            "clocks": clk, "note": "not the timed region; per-rank figures, rank 0 printed" if world > 1 else
+            "not the timed region"}
 
 
 def run_e2e(args, wl, step, stream, total_flops, world, device):
@@ -623,12 +742,13 @@ def run_e2e(args, wl, step, stream, total_flops, world, device):
             t = t.view(dtype)
         return t.pin_memory()
     h_in = [pinned(wl.x.view(np.int16), torch.bfloat16), pinned(wl.w.view(np.int16), torch.bfloat16),
-            pinned(wl.dy.view(np.int16), torch.bfloat16), pinned(wl.moe_x.view(np.int16), torch.bfloat16),
+            pinned(wl.dy.view(np.int16), torch.bfloat16), pinned(wl.xw.view(np.int16), torch.bfloat16),
+            pinned(wl.moe_x.view(np.int16), torch.bfloat16),
             pinned(wl.moe_w.view(np.int16), torch.bfloat16), pinned(wl.moe_offsets)]
     sets = [step, DeviceStep(wl, device)]
 
     def dev_in(st):
-        return [st.x, st.w, st.dy, st.moe_x, st.moe_w, st.moe_off]
+        return [st.x, st.w, st.dy, st.xw, st.moe_x, st.moe_w, st.moe_off]
 
     def dev_out(st):
         return [st.y, st.dx, st.dw, st.moe_y]

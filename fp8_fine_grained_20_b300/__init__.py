@@ -24,6 +24,11 @@ Functions (same names as the C entry points):
   its bf16 output 1x128-quantized in the epilogue -> (codes, scales)
 * ``fp8_grouped_gemm_blockscaled(A, sA, B, sB, offsets)`` -- MoE experts
   (xn--jj0bz6z98ct0a29q.com post 362465: FP8-dispatched activations)
+* ``*_pow2`` quantizers -- power-of-two scales (the smallest 2^e >= amax/448;
+  why-be.why-be.co.kr post 55081 and sunipension.com post 314414: scaling
+  factors that are integral powers of 2), and ``fp8_gemm_blockscaled_mx`` /
+  ``fp8_grouped_gemm_blockscaled_mx``, which take such scales and let the
+  tensor core apply them (no FP32 promotion)
 
 Scale tensors are logical 2-D tensors with arbitrary strides; the default
 outputs are "MN-major" views (stride 1 along the row/column index), the layout
@@ -42,6 +47,9 @@ __all__ = [
     "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_q1x128", "fp8_grouped_gemm_blockscaled",
     "fp8_get_device_status", "fp8_status_string", "fp8_selftest_bounded_wait",
     "fp8_mma_accumulation_probe",
+    "fp8_quant_act_1x128_pow2", "fp8_quant_w_128x128_pow2", "fp8_quant_w_128x128_batched_pow2",
+    "fp8_requant_1x128_to_128x1_pow2", "fp8_gemm_blockscaled_mx", "fp8_grouped_gemm_blockscaled_mx",
+    "fp8_selftest_gemm_timeout", "fp8_swiglu_quant_1x128",
     "FP8_KMAJOR_NK", "FP8_ROWMAJOR_KN", "FP8_SB_BLOCK128x128", "FP8_SB_COL128x1",
 ]
 
@@ -57,6 +65,7 @@ FP8_SB_COL128x1 = 1
 STATUS_NAMES = {
     0: "FP8_OK", 1: "FP8_ERR_NULL", 2: "FP8_ERR_ALIGN", 3: "FP8_ERR_SHAPE", 4: "FP8_ERR_CUDA",
     5: "FP8_ERR_DEVICE_TIMEOUT", 6: "FP8_ERR_ARG", 7: "FP8_ERR_DEVICE", 8: "FP8_ERR_DEVICE_GROUPS",
+    9: "FP8_ERR_DEVICE_SCALES",
 }
 
 # (name, argtypes) of every exported function; restype fp8_status_t (int) unless noted
@@ -74,6 +83,18 @@ _SIGNATURES = {
                                     _vp, _i64, _i64, _i64, _i64, _i64, _vp],
     "fp8_grouped_gemm_blockscaled": [_vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _int, _i64, _i64, _i64,
                                      _vp, _i64, _vp],
+    "fp8_quant_act_1x128_pow2": [_vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp],
+    "fp8_quant_w_128x128_pow2": [_vp, _i64, _i64, _i64, _vp, _i64, _int, _vp, _i64, _i64, _vp],
+    "fp8_quant_w_128x128_batched_pow2": [_vp, _i64, _i64, _i64, _i64, _i64, _vp, _i64, _i64, _int, _vp, _i64,
+                                         _i64, _i64, _vp],
+    "fp8_requant_1x128_to_128x1_pow2": [_vp, _i64, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64,
+                                        _vp],
+    "fp8_gemm_blockscaled_mx": [_vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _int, _vp, _i64,
+                                _i64, _i64, _i64, _vp],
+    "fp8_grouped_gemm_blockscaled_mx": [_vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp, _int, _i64, _i64, _i64,
+                                        _vp, _i64, _vp],
+    "fp8_selftest_gemm_timeout": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, ctypes.c_uint64, _vp],
+    "fp8_swiglu_quant_1x128": [_vp, _i64, _vp, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _i64, _vp, _i64, _vp],
     "fp8_get_device_status": [_vp, ctypes.POINTER(ctypes.c_int32), _int],
     "fp8_selftest_bounded_wait": [ctypes.c_uint64, _vp],
     "fp8_mma_accumulation_probe": [_vp, _vp, _i64, _vp, _vp],
@@ -153,6 +174,50 @@ def _scale_out(rows, cols, layout, device):
 def fp8_quant_act_1x128(x, q=None, s=None, *, scale_layout="mn", stream=None):
     """1x128 activation quantization.  x: bf16 [M, K] (K % 128 == 0).
     Returns (q uint8 [M, K], s float32 logical [M, K/128])."""
+    return _quant_act(x, q, s, scale_layout, stream, "fp8_quant_act_1x128")
+
+
+def fp8_swiglu_quant_1x128(gate, up=None, q=None, s=None, y=None, *, scale_layout="mn", write_y=False,
+                           stream=None):
+    """SwiGLU recompute fused with 1x128 quantization.  gate, up: bf16 [M, F]
+    (unit inner stride; F % 128 == 0); with up=None, `gate` is the fused
+    [M, 2F] gate/up output and is split in halves.  Returns (q uint8 [M, F],
+    s float32 logical [M, F/128]) and, with write_y=True or y given, also the
+    bf16 SwiGLU values y [M, F]."""
+    _need_cuda(gate)
+    if up is None:
+        F2 = gate.shape[1]
+        gate, up = gate[:, :F2 // 2], gate[:, F2 // 2:]
+    _need_cuda(up)
+    _row_major(gate, "gate")
+    _row_major(up, "up")
+    if gate.dtype != torch.bfloat16 or up.dtype != torch.bfloat16 or gate.shape != up.shape:
+        raise TypeError("gate and up must be bfloat16 tensors of one shape")
+    M, F = gate.shape
+    if q is None:
+        q = torch.empty((M, F), dtype=torch.uint8, device=gate.device)
+    if s is None:
+        s = _scale_out(M, F // 128, scale_layout, gate.device)
+    if y is None and write_y:
+        y = torch.empty((M, F), dtype=torch.bfloat16, device=gate.device)
+    _need_cuda(q, s)
+    _row_major(q, "q")
+    if y is not None:
+        _need_cuda(y)
+        _row_major(y, "y")
+    _check(capi().fp8_swiglu_quant_1x128(_ptr(gate), gate.stride(0), _ptr(up), up.stride(0), M, F,
+                                         _ptr(q), q.stride(0), _ptr(s), s.stride(0), s.stride(1),
+                                         _ptr(y) if y is not None else None, y.stride(0) if y is not None else 0,
+                                         _stream(stream)), "fp8_swiglu_quant_1x128")
+    return (q, s, y) if y is not None else (q, s)
+
+
+def fp8_quant_act_1x128_pow2(x, q=None, s=None, *, scale_layout="mn", stream=None):
+    """fp8_quant_act_1x128 with power-of-two scales (smallest 2^e >= amax/448)."""
+    return _quant_act(x, q, s, scale_layout, stream, "fp8_quant_act_1x128_pow2")
+
+
+def _quant_act(x, q, s, scale_layout, stream, name):
     _need_cuda(x)
     _row_major(x, "x")
     if x.dtype != torch.bfloat16:
@@ -164,9 +229,8 @@ def fp8_quant_act_1x128(x, q=None, s=None, *, scale_layout="mn", stream=None):
         s = _scale_out(M, K // 128, scale_layout, x.device)
     _need_cuda(q, s)
     _row_major(q, "q")
-    _check(capi().fp8_quant_act_1x128(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s),
-                                      s.stride(0), s.stride(1), _stream(stream)),
-           "fp8_quant_act_1x128")
+    _check(getattr(capi(), name)(_ptr(x), M, K, x.stride(0), _ptr(q), q.stride(0), _ptr(s),
+                                 s.stride(0), s.stride(1), _stream(stream)), name)
     return q, s
 
 
@@ -174,6 +238,15 @@ def fp8_quant_w_128x128(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, stream=Non
     """128x128 weight quantization.  w: bf16 [K, N].  Returns (q, s) with q
     uint8 [N, K] for FP8_KMAJOR_NK (default) or [K, N] for FP8_ROWMAJOR_KN and
     s float32 [K/128, N/128]."""
+    return _quant_w(w, q, s, q_layout, stream, "fp8_quant_w_128x128")
+
+
+def fp8_quant_w_128x128_pow2(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, stream=None):
+    """fp8_quant_w_128x128 with power-of-two scales."""
+    return _quant_w(w, q, s, q_layout, stream, "fp8_quant_w_128x128_pow2")
+
+
+def _quant_w(w, q, s, q_layout, stream, name):
     _need_cuda(w)
     _row_major(w, "w")
     if w.dtype != torch.bfloat16:
@@ -186,9 +259,8 @@ def fp8_quant_w_128x128(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, stream=Non
         s = torch.empty((K // 128, N // 128), dtype=torch.float32, device=w.device)
     _need_cuda(q, s)
     _row_major(q, "q")
-    _check(capi().fp8_quant_w_128x128(_ptr(w), K, N, w.stride(0), _ptr(q), q.stride(0), int(q_layout),
-                                      _ptr(s), s.stride(0), s.stride(1), _stream(stream)),
-           "fp8_quant_w_128x128")
+    _check(getattr(capi(), name)(_ptr(w), K, N, w.stride(0), _ptr(q), q.stride(0), int(q_layout),
+                                 _ptr(s), s.stride(0), s.stride(1), _stream(stream)), name)
     return q, s
 
 
@@ -197,6 +269,15 @@ def fp8_quant_w_128x128_batched(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, st
     (each weight row-major, any expert stride).  Returns (q, s) with q uint8
     [G, N, K] for FP8_KMAJOR_NK (default) or [G, K, N] for FP8_ROWMAJOR_KN and
     s float32 [G, K/128, N/128]."""
+    return _quant_w_batched(w, q, s, q_layout, stream, "fp8_quant_w_128x128_batched")
+
+
+def fp8_quant_w_128x128_batched_pow2(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, stream=None):
+    """fp8_quant_w_128x128_batched with power-of-two scales."""
+    return _quant_w_batched(w, q, s, q_layout, stream, "fp8_quant_w_128x128_batched_pow2")
+
+
+def _quant_w_batched(w, q, s, q_layout, stream, name):
     _need_cuda(w)
     if w.dim() != 3 or w.stride(2) != 1:
         raise ValueError("w must be a 3-D tensor with unit stride along its last dimension")
@@ -211,16 +292,24 @@ def fp8_quant_w_128x128_batched(w, q=None, s=None, *, q_layout=FP8_KMAJOR_NK, st
     _need_cuda(q, s)
     if q.dim() != 3 or q.stride(2) != 1 or s.dim() != 3:
         raise ValueError("q must be 3-D with unit inner stride and s 3-D")
-    _check(capi().fp8_quant_w_128x128_batched(_ptr(w), G, K, N, w.stride(1), w.stride(0), _ptr(q), q.stride(1),
-                                              q.stride(0), int(q_layout), _ptr(s), s.stride(1), s.stride(2),
-                                              s.stride(0), _stream(stream)),
-           "fp8_quant_w_128x128_batched")
+    _check(getattr(capi(), name)(_ptr(w), G, K, N, w.stride(1), w.stride(0), _ptr(q), q.stride(1),
+                                 q.stride(0), int(q_layout), _ptr(s), s.stride(1), s.stride(2),
+                                 s.stride(0), _stream(stream)), name)
     return q, s
 
 
 def fp8_requant_1x128_to_128x1(q, s, qT=None, sT=None, *, scale_layout="mn", stream=None):
     """1x128 -> 128x1 requantization.  q uint8 [M, K], s logical [M, K/128].
     Returns (qT uint8 [K, M], sT float32 logical [K, M/128])."""
+    return _requant(q, s, qT, sT, scale_layout, stream, "fp8_requant_1x128_to_128x1")
+
+
+def fp8_requant_1x128_to_128x1_pow2(q, s, qT=None, sT=None, *, scale_layout="mn", stream=None):
+    """fp8_requant_1x128_to_128x1 with power-of-two scales for the 128x1 groups."""
+    return _requant(q, s, qT, sT, scale_layout, stream, "fp8_requant_1x128_to_128x1_pow2")
+
+
+def _requant(q, s, qT, sT, scale_layout, stream, name):
     _need_cuda(q, s)
     _row_major(q, "q")
     M, K = q.shape
@@ -232,16 +321,25 @@ def fp8_requant_1x128_to_128x1(q, s, qT=None, sT=None, *, scale_layout="mn", str
         sT = _scale_out(K, M // 128, scale_layout, q.device)
     _need_cuda(qT, sT)
     _row_major(qT, "qT")
-    _check(capi().fp8_requant_1x128_to_128x1(_ptr(q), M, K, q.stride(0), _ptr(s), s.stride(0), s.stride(1),
-                                             _ptr(qT), qT.stride(0), _ptr(sT), sT.stride(0), sT.stride(1),
-                                             _stream(stream)),
-           "fp8_requant_1x128_to_128x1")
+    _check(getattr(capi(), name)(_ptr(q), M, K, q.stride(0), _ptr(s), s.stride(0), s.stride(1),
+                                 _ptr(qT), qT.stride(0), _ptr(sT), sT.stride(0), sT.stride(1),
+                                 _stream(stream)), name)
     return qT, sT
 
 
 def fp8_gemm_blockscaled(A, sA, B, sB, sb_kind=FP8_SB_BLOCK128x128, out=None, *, stream=None):
     """C bf16 [M, N] = block-scaled A [M, K] x B [N, K]^T.
     sA logical [M, K/128]; sB logical [K/128, N/128] (block) or [K/128, N] (per column)."""
+    return _gemm(A, sA, B, sB, sb_kind, out, stream, "fp8_gemm_blockscaled")
+
+
+def fp8_gemm_blockscaled_mx(A, sA, B, sB, sb_kind=FP8_SB_BLOCK128x128, out=None, *, stream=None):
+    """fp8_gemm_blockscaled with power-of-two scales applied by the tensor core
+    (every scale a power of two, e.g. from the _pow2 quantizers)."""
+    return _gemm(A, sA, B, sB, sb_kind, out, stream, "fp8_gemm_blockscaled_mx")
+
+
+def _gemm(A, sA, B, sB, sb_kind, out, stream, name):
     _need_cuda(A, sA, B, sB)
     _row_major(A, "A")
     _row_major(B, "B")
@@ -253,10 +351,9 @@ def fp8_gemm_blockscaled(A, sA, B, sB, sb_kind=FP8_SB_BLOCK128x128, out=None, *,
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
     _need_cuda(out)
     _row_major(out, "out")
-    _check(capi().fp8_gemm_blockscaled(_ptr(A), A.stride(0), _ptr(sA), sA.stride(0), sA.stride(1),
-                                       _ptr(B), B.stride(0), _ptr(sB), sB.stride(0), sB.stride(1),
-                                       int(sb_kind), _ptr(out), out.stride(0), M, N, K, _stream(stream)),
-           "fp8_gemm_blockscaled")
+    _check(getattr(capi(), name)(_ptr(A), A.stride(0), _ptr(sA), sA.stride(0), sA.stride(1),
+                                 _ptr(B), B.stride(0), _ptr(sB), sB.stride(0), sB.stride(1),
+                                 int(sb_kind), _ptr(out), out.stride(0), M, N, K, _stream(stream)), name)
     return out
 
 
@@ -289,6 +386,15 @@ def fp8_grouped_gemm_blockscaled(A, sA, B, sB, offsets, out=None, *, stream=None
     """Grouped GEMM.  A uint8 [M_total, K], sA logical [M_total, K/128]; B uint8
     [G, N, K] dense; sB float32 [G, K/128, N/128] dense; offsets int32 CUDA
     [G+1].  Returns C bf16 [M_total, N] (rows outside every expert untouched)."""
+    return _grouped(A, sA, B, sB, offsets, out, stream, "fp8_grouped_gemm_blockscaled")
+
+
+def fp8_grouped_gemm_blockscaled_mx(A, sA, B, sB, offsets, out=None, *, stream=None):
+    """fp8_grouped_gemm_blockscaled with power-of-two scales applied by the tensor core."""
+    return _grouped(A, sA, B, sB, offsets, out, stream, "fp8_grouped_gemm_blockscaled_mx")
+
+
+def _grouped(A, sA, B, sB, offsets, out, stream, name):
     _need_cuda(A, sA, B, sB, offsets)
     _row_major(A, "A")
     if not (B.is_contiguous() and sB.is_contiguous() and offsets.is_contiguous()):
@@ -303,10 +409,9 @@ def fp8_grouped_gemm_blockscaled(A, sA, B, sB, offsets, out=None, *, stream=None
         out = torch.empty((M_total, N), dtype=torch.bfloat16, device=A.device)
     _need_cuda(out)
     _row_major(out, "out")
-    _check(capi().fp8_grouped_gemm_blockscaled(_ptr(A), A.stride(0), _ptr(sA), sA.stride(0), sA.stride(1),
-                                               _ptr(B), _ptr(sB), _ptr(offsets), G, M_total, N, K,
-                                               _ptr(out), out.stride(0), _stream(stream)),
-           "fp8_grouped_gemm_blockscaled")
+    _check(getattr(capi(), name)(_ptr(A), A.stride(0), _ptr(sA), sA.stride(0), sA.stride(1),
+                                 _ptr(B), _ptr(sB), _ptr(offsets), G, M_total, N, K,
+                                 _ptr(out), out.stride(0), _stream(stream)), name)
     return out
 
 
@@ -322,6 +427,25 @@ def fp8_selftest_bounded_wait(timeout_ns=1000000, stream=None):
     """Run the bounded-wait self-test kernel (a wait that nothing satisfies);
     afterwards the device status word holds FP8_ERR_DEVICE_TIMEOUT (5)."""
     _check(capi().fp8_selftest_bounded_wait(int(timeout_ns), _stream(stream)), "fp8_selftest_bounded_wait")
+
+
+def fp8_selftest_gemm_timeout(A, sA, B, sB, out=None, *, wait_ns=2000000, stream=None):
+    """Run the GEMM failure-path self-test: fp8_gemm_blockscaled on dense A
+    uint8 [M, K], sA float32 MN-major view [M, K/128] (sA.stride(0) == 1), B uint8
+    [N, K], sB float32 [K/128, N/128], with every pipeline wait bounded by
+    wait_ns and all loads after the first K-block withheld.  Afterwards the
+    device status word holds FP8_ERR_DEVICE_TIMEOUT (5); `out` is undefined."""
+    _need_cuda(A, sA, B, sB)
+    M, K = A.shape
+    N = B.shape[0]
+    if not (A.is_contiguous() and B.is_contiguous() and sB.is_contiguous() and sA.stride(0) == 1
+            and sA.stride(1) == M):
+        raise ValueError("dense operands and an MN-major sA are required")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check(capi().fp8_selftest_gemm_timeout(_ptr(A), _ptr(sA), _ptr(B), _ptr(sB), _ptr(out), M, N, K,
+                                            int(wait_ns), _stream(stream)), "fp8_selftest_gemm_timeout")
+    return out
 
 
 def fp8_mma_accumulation_probe(A, B, out=None, *, stream=None):

@@ -11,8 +11,10 @@
 
 #include "../../include/fp8fg.h"
 #include "gemm.cuh"
+#include "gemm_mx.cuh"
 #include "probe.cuh"
 #include "quant.cuh"
+#include "swiglu.cuh"
 
 namespace {
 
@@ -116,19 +118,21 @@ bool allow_smem(K kernel, size_t bytes, int dev, int* done) {
     return true;
 }
 
-template <int SBK, bool GROUPED, bool QOUT = false>
-fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const uint8_t* B, int64_t ldb,
-                         int64_t b_rows, const gemm::Args& args, cudaStream_t stream,
-                         const gemm::QArgs& qargs = gemm::QArgs{}) {
-    static int attr_set[kMaxDevices] = {0};
-    static int max_pairs[kMaxDevices] = {0};
+// Launch state of one CTA-pair GEMM kernel, per device: the shared-memory
+// attribute is set once and the number of co-resident pairs is cached.
+struct PairLaunch {
+    int ready[kMaxDevices];
+    int max_pairs[kMaxDevices];
+};
+
+// Configure a persistent CTA-pair launch of `kernel` (clusters of 2 along x):
+// one pair per co-resident cluster slot, never more pairs than tiles.
+template <typename KernelT>
+fp8_status_t pair_config(KernelT kernel, size_t smem, PairLaunch& st, const gemm::Args& args, bool grouped,
+                         cudaStream_t stream, cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attr) {
     const int dev = current_device();
     if (dev < 0 || dev >= kMaxDevices) return FP8_ERR_CUDA;
-    auto kernel = gemm::k_gemm_blockscaled<SBK, GROUPED, QOUT>;
-    const size_t smem = GROUPED ? gemm::SMEM_GROUPED : gemm::SMEM_PLAIN;
-
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cfg = cudaLaunchConfig_t{};
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
@@ -138,31 +142,64 @@ fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const ui
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (!attr_set[dev]) {
+    if (!st.ready[dev]) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess)
             return FP8_ERR_DEVICE;
-        // co-resident CTA pairs: the persistent grid never exceeds this
         int n = 0;
         cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count(dev)), 1, 1);
         if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
             cudaGetLastError();
             return FP8_ERR_DEVICE;
         }
-        max_pairs[dev] = n;
-        attr_set[dev] = 1;
+        st.max_pairs[dev] = n;
+        st.ready[dev] = 1;
     }
-    CUtensorMap tmA, tmB;
-    if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
-    if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BNH)) return FP8_ERR_CUDA;
     // the grouped pair-row count is known only on the device: bound it by the
     // padded rows, each expert adding at most one half-empty pair-row
     int64_t pair_rows = (args.m_blocks + 1) / 2;
-    if (GROUPED) pair_rows = std::min<int64_t>(args.m_blocks, (args.m_blocks + args.G + 1) / 2);
+    if (grouped) pair_rows = std::min<int64_t>(args.m_blocks, (args.m_blocks + args.G + 1) / 2);
     const int64_t tiles = pair_rows * args.n_blocks;
-    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(tiles, max_pairs[dev]));
+    const int64_t pairs = std::max<int64_t>(1, std::min<int64_t>(tiles, st.max_pairs[dev]));
     cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    return FP8_OK;
+}
+
+template <int SBK, bool GROUPED, bool QOUT = false>
+fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const uint8_t* B, int64_t ldb,
+                         int64_t b_rows, const gemm::Args& args, cudaStream_t stream,
+                         const gemm::QArgs& qargs = gemm::QArgs{}) {
+    static PairLaunch st = {};
+    auto kernel = gemm::k_gemm_blockscaled<SBK, GROUPED, QOUT>;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    const fp8_status_t rc =
+        pair_config(kernel, GROUPED ? gemm::SMEM_GROUPED : gemm::SMEM_PLAIN, st, args, GROUPED, stream, cfg, attr);
+    if (rc != FP8_OK) return rc;
+    CUtensorMap tmA, tmB;
+    if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
+    if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BNH)) return FP8_ERR_CUDA;
     if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args, qargs) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8_ERR_CUDA;
+    }
+    return launch_status();
+}
+
+template <int SBK, bool GROUPED>
+fp8_status_t launch_gemm_mx(const uint8_t* A, int64_t lda, int64_t a_rows, const uint8_t* B, int64_t ldb,
+                            int64_t b_rows, const gemm::Args& args, cudaStream_t stream) {
+    static PairLaunch st = {};
+    auto kernel = gemm::k_gemm_mx<SBK, GROUPED>;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    const fp8_status_t rc = pair_config(kernel, GROUPED ? gemm::MX_SMEM_GROUPED : gemm::MX_SMEM_PLAIN, st, args,
+                                        GROUPED, stream, cfg, attr);
+    if (rc != FP8_OK) return rc;
+    CUtensorMap tmA, tmB;
+    if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
+    if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BNH)) return FP8_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args) != cudaSuccess) {
         cudaGetLastError();
         return FP8_ERR_CUDA;
     }
@@ -197,6 +234,7 @@ const char* fp8_status_string(fp8_status_t s) {
         case FP8_ERR_ARG: return "FP8_ERR_ARG: invalid enum or stride argument";
         case FP8_ERR_DEVICE: return "FP8_ERR_DEVICE: unsupported device or resource limit";
         case FP8_ERR_DEVICE_GROUPS: return "FP8_ERR_DEVICE_GROUPS: invalid group offsets seen on the device";
+        case FP8_ERR_DEVICE_SCALES: return "FP8_ERR_DEVICE_SCALES: a scale given to an _mx GEMM is not a power of two";
     }
     return "unknown fp8fg status";
 }
@@ -235,8 +273,13 @@ fp8_status_t fp8_mma_accumulation_probe(const uint8_t* A, const uint8_t* B, int6
     return launch_status();
 }
 
-fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
-                                 float* s, int64_t s_stride_m, int64_t s_stride_kb, void* stream) {
+}  // extern "C"
+
+namespace {
+
+template <bool POW2>
+fp8_status_t quant_act_entry(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                             float* s, int64_t s_stride_m, int64_t s_stride_kb, void* stream) {
     if (M < 0 || K < 0 || K % 128) return FP8_ERR_SHAPE;
     if (M == 0 || K == 0) return FP8_OK;
     if (!x || !q || !s) return FP8_ERR_NULL;
@@ -250,7 +293,7 @@ fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_
     const int sms = sm_count(dev);
     if (sms <= 0) return FP8_ERR_CUDA;
     constexpr int UNROLL = 2;
-    auto kernel = k_quant_act_1x128<UNROLL>;
+    auto kernel = k_quant_act_1x128<UNROLL, POW2>;
     const int per_sm = blocks_per_sm(kernel, 256, dev, occ);
     const int64_t slots = ceil_div(M * KB, 8);           // a warp quantizes 8 groups per slot
     const int64_t want = ceil_div(slots, 8 * UNROLL);    // 8 warps per CTA, UNROLL slots each
@@ -261,10 +304,10 @@ fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_
     return launch_status();
 }
 
-fp8_status_t fp8_quant_w_128x128_batched(const uint16_t* w, int64_t G, int64_t K, int64_t N, int64_t ldw,
-                                         int64_t w_batch_stride, uint8_t* q, int64_t ldq, int64_t q_batch_stride,
-                                         int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb,
-                                         int64_t s_batch_stride, void* stream) {
+template <bool POW2>
+fp8_status_t quant_w_entry(const uint16_t* w, int64_t G, int64_t K, int64_t N, int64_t ldw, int64_t w_batch_stride,
+                           uint8_t* q, int64_t ldq, int64_t q_batch_stride, int q_layout, float* s,
+                           int64_t s_stride_kb, int64_t s_stride_nb, int64_t s_batch_stride, void* stream) {
     if (G < 0 || K < 0 || N < 0 || K % 128 || N % 128) return FP8_ERR_SHAPE;
     if (q_layout != FP8_KMAJOR_NK && q_layout != FP8_ROWMAJOR_KN) return FP8_ERR_ARG;
     if (G == 0 || K == 0 || N == 0) return FP8_OK;
@@ -283,7 +326,7 @@ fp8_status_t fp8_quant_w_128x128_batched(const uint16_t* w, int64_t G, int64_t K
     const int dev = current_device();
     const int sms = sm_count(dev);
     if (sms <= 0) return FP8_ERR_CUDA;
-    if (!allow_smem(k_quant_w_128x128, WQ_SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
+    if (!allow_smem(k_quant_w_128x128<POW2>, WQ_SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
     CUtensorMap tm;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(G)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(ldw * 2),
@@ -305,19 +348,14 @@ fp8_status_t fp8_quant_w_128x128_batched(const uint16_t* w, int64_t G, int64_t K
     const int64_t blocks = G * KB * NB;
     const int64_t cap = 2 * static_cast<int64_t>(sms);
     const int grid = static_cast<int>(blocks < cap ? blocks : cap);
-    k_quant_w_128x128<<<grid, WQ_THREADS, WQ_SMEM, as_stream(stream)>>>(tm, a);
+    k_quant_w_128x128<POW2><<<grid, WQ_THREADS, WQ_SMEM, as_stream(stream)>>>(tm, a);
     return launch_status();
 }
 
-fp8_status_t fp8_quant_w_128x128(const uint16_t* w, int64_t K, int64_t N, int64_t ldw, uint8_t* q, int64_t ldq,
-                                 int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb, void* stream) {
-    return fp8_quant_w_128x128_batched(w, 1, K, N, ldw, 0, q, ldq, 0, q_layout, s, s_stride_kb, s_stride_nb, 0,
-                                       stream);
-}
-
-fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, int64_t ldq, const float* s,
-                                        int64_t s_stride_m, int64_t s_stride_kb, uint8_t* qT, int64_t ldqT,
-                                        float* sT, int64_t sT_stride_k, int64_t sT_stride_mb, void* stream) {
+template <bool POW2>
+fp8_status_t requant_entry(const uint8_t* q, int64_t M, int64_t K, int64_t ldq, const float* s, int64_t s_stride_m,
+                           int64_t s_stride_kb, uint8_t* qT, int64_t ldqT, float* sT, int64_t sT_stride_k,
+                           int64_t sT_stride_mb, void* stream) {
     if (M < 0 || K < 0 || M % 128 || K % 128) return FP8_ERR_SHAPE;
     if (M == 0 || K == 0) return FP8_OK;
     if (!q || !s || !qT || !sT) return FP8_ERR_NULL;
@@ -332,7 +370,7 @@ fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, 
     const int dev = current_device();
     const int sms = sm_count(dev);
     if (sms <= 0) return FP8_ERR_CUDA;
-    if (!allow_smem(k_requant_1x128_to_128x1, RQ_SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
+    if (!allow_smem(k_requant_1x128_to_128x1<POW2>, RQ_SMEM, dev, smem_ok)) return FP8_ERR_DEVICE;
     CUtensorMap tm;   // 128 x 128 code blocks, 128-byte swizzle
     if (!make_kmajor_map(&tm, q, M, K, ldq, 128)) return FP8_ERR_CUDA;
     RequantArgs a{};
@@ -348,20 +386,122 @@ fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, 
     a.KB = static_cast<int>(KB);
     const int64_t cap = 2 * static_cast<int64_t>(sms);
     const int grid = static_cast<int>(MB * KB < cap ? MB * KB : cap);
-    k_requant_1x128_to_128x1<<<grid, RQ_THREADS, RQ_SMEM, as_stream(stream)>>>(tm, a);
+    k_requant_1x128_to_128x1<POW2><<<grid, RQ_THREADS, RQ_SMEM, as_stream(stream)>>>(tm, a);
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8_status_t fp8_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                                 float* s, int64_t s_stride_m, int64_t s_stride_kb, void* stream) {
+    return quant_act_entry<false>(x, M, K, ldx, q, ldq, s, s_stride_m, s_stride_kb, stream);
+}
+
+fp8_status_t fp8_swiglu_quant_1x128(const uint16_t* gate, int64_t ldg, const uint16_t* up, int64_t ldu, int64_t M,
+                                    int64_t F, uint8_t* q, int64_t ldq, float* s, int64_t s_stride_m,
+                                    int64_t s_stride_fb, uint16_t* y, int64_t ldy, void* stream) {
+    if (M < 0 || F < 0 || F % 128) return FP8_ERR_SHAPE;
+    if (M == 0 || F == 0) return FP8_OK;
+    if (!gate || !up || !q || !s) return FP8_ERR_NULL;
+    if (ldg < F || ldu < F || ldq < F || s_stride_m < 0 || s_stride_fb < 0 || (y && ldy < F)) return FP8_ERR_ARG;
+    if (!aligned16(gate) || !aligned16(up) || !aligned16(q) || (ldg * 2) % 16 || (ldu * 2) % 16 || ldq % 16 ||
+        (reinterpret_cast<uintptr_t>(s) & 3u) || (y && (!aligned16(y) || (ldy * 2) % 16)))
+        return FP8_ERR_ALIGN;
+    const int64_t FB = F / 128;
+    if (M > INT32_MAX || M * FB > (int64_t(1) << 40)) return FP8_ERR_SHAPE;
+    static int occ[kMaxDevices] = {0};
+    const int dev = current_device();
+    const int sms = sm_count(dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    constexpr int UNROLL = 2;
+    auto kernel = k_swiglu_quant_1x128<UNROLL>;
+    const int per_sm = blocks_per_sm(kernel, 256, dev, occ);
+    const int64_t slots = ceil_div(M * FB, 8);
+    const int64_t want = ceil_div(slots, 8 * UNROLL);
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    const int grid = static_cast<int>(want < cap ? want : cap);
+    SwigluArgs a{};
+    a.g = gate;
+    a.ldg = ldg;
+    a.u = up;
+    a.ldu = ldu;
+    a.q = q;
+    a.ldq = ldq;
+    a.s = s;
+    a.ssm = s_stride_m;
+    a.ssfb = s_stride_fb;
+    a.y = y;
+    a.ldy = ldy;
+    a.M = static_cast<int>(M);
+    a.FB = static_cast<int>(FB);
+    kernel<<<grid, 256, 0, as_stream(stream)>>>(a);
+    return launch_status();
+}
+
+fp8_status_t fp8_quant_act_1x128_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                                      int64_t ldq, float* s, int64_t s_stride_m, int64_t s_stride_kb, void* stream) {
+    return quant_act_entry<true>(x, M, K, ldx, q, ldq, s, s_stride_m, s_stride_kb, stream);
+}
+
+fp8_status_t fp8_quant_w_128x128_batched(const uint16_t* w, int64_t G, int64_t K, int64_t N, int64_t ldw,
+                                         int64_t w_batch_stride, uint8_t* q, int64_t ldq, int64_t q_batch_stride,
+                                         int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb,
+                                         int64_t s_batch_stride, void* stream) {
+    return quant_w_entry<false>(w, G, K, N, ldw, w_batch_stride, q, ldq, q_batch_stride, q_layout, s, s_stride_kb,
+                                s_stride_nb, s_batch_stride, stream);
+}
+
+fp8_status_t fp8_quant_w_128x128_batched_pow2(const uint16_t* w, int64_t G, int64_t K, int64_t N, int64_t ldw,
+                                              int64_t w_batch_stride, uint8_t* q, int64_t ldq,
+                                              int64_t q_batch_stride, int q_layout, float* s, int64_t s_stride_kb,
+                                              int64_t s_stride_nb, int64_t s_batch_stride, void* stream) {
+    return quant_w_entry<true>(w, G, K, N, ldw, w_batch_stride, q, ldq, q_batch_stride, q_layout, s, s_stride_kb,
+                               s_stride_nb, s_batch_stride, stream);
+}
+
+fp8_status_t fp8_quant_w_128x128(const uint16_t* w, int64_t K, int64_t N, int64_t ldw, uint8_t* q, int64_t ldq,
+                                 int q_layout, float* s, int64_t s_stride_kb, int64_t s_stride_nb, void* stream) {
+    return quant_w_entry<false>(w, 1, K, N, ldw, 0, q, ldq, 0, q_layout, s, s_stride_kb, s_stride_nb, 0, stream);
+}
+
+fp8_status_t fp8_quant_w_128x128_pow2(const uint16_t* w, int64_t K, int64_t N, int64_t ldw, uint8_t* q,
+                                      int64_t ldq, int q_layout, float* s, int64_t s_stride_kb,
+                                      int64_t s_stride_nb, void* stream) {
+    return quant_w_entry<true>(w, 1, K, N, ldw, 0, q, ldq, 0, q_layout, s, s_stride_kb, s_stride_nb, 0, stream);
+}
+
+fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, int64_t ldq, const float* s,
+                                        int64_t s_stride_m, int64_t s_stride_kb, uint8_t* qT, int64_t ldqT,
+                                        float* sT, int64_t sT_stride_k, int64_t sT_stride_mb, void* stream) {
+    return requant_entry<false>(q, M, K, ldq, s, s_stride_m, s_stride_kb, qT, ldqT, sT, sT_stride_k, sT_stride_mb,
+                                stream);
+}
+
+fp8_status_t fp8_requant_1x128_to_128x1_pow2(const uint8_t* q, int64_t M, int64_t K, int64_t ldq, const float* s,
+                                             int64_t s_stride_m, int64_t s_stride_kb, uint8_t* qT, int64_t ldqT,
+                                             float* sT, int64_t sT_stride_k, int64_t sT_stride_mb, void* stream) {
+    return requant_entry<true>(q, M, K, ldq, s, s_stride_m, s_stride_kb, qT, ldqT, sT, sT_stride_k, sT_stride_mb,
+                               stream);
 }
 
 }  // extern "C"
 
 namespace {
 
-// Validation and launch shared by the bf16 and the quantizing epilogue.
+// Which kernel a GEMM entry point runs.
+enum class GemmKind { kPromote, kPromoteQuantOut, kMx };
+
+// Validation and launch shared by the bf16 epilogue, the quantizing epilogue
+// and the power-of-two (hardware-scaled) kernel.  wait_ns / withhold: the
+// pipeline-wait bound and the test-only withholding of TMA loads.
 fp8_status_t gemm_entry(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
                         const uint8_t* B, int64_t ldb, const float* sB, int64_t sb_stride_kb, int64_t sb_stride_n,
                         int sb_kind, uint16_t* C, int64_t ldc, uint8_t* Cq, int64_t ldcq, float* sC,
-                        int64_t sc_stride_m, int64_t sc_stride_nb, int64_t M, int64_t N, int64_t K, bool qout,
-                        cudaStream_t stream) {
+                        int64_t sc_stride_m, int64_t sc_stride_nb, int64_t M, int64_t N, int64_t K, GemmKind kind,
+                        cudaStream_t stream, uint64_t wait_ns = kWaitTimeoutNs, int withhold = 0) {
+    const bool qout = kind == GemmKind::kPromoteQuantOut;
     if (sb_kind != FP8_SB_BLOCK128x128 && sb_kind != FP8_SB_COL128x1) return FP8_ERR_ARG;
     if (M < 0 || N < 0 || K < 0 || M % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
     if (M == 0 || N == 0) return FP8_OK;
@@ -397,6 +537,12 @@ fp8_status_t gemm_entry(const uint8_t* A, int64_t lda, const float* sA, int64_t 
     a.sb_cols = static_cast<int>(sb_kind == FP8_SB_COL128x1 ? N : N / 128);
     a.offsets = nullptr;
     a.G = 0;
+    a.wait_ns = wait_ns;
+    a.withhold = withhold;
+    if (kind == GemmKind::kMx) {
+        if (sb_kind == FP8_SB_COL128x1) return launch_gemm_mx<gemm::SB_COL, false>(A, lda, M, B, ldb, N, a, stream);
+        return launch_gemm_mx<gemm::SB_BLOCK, false>(A, lda, M, B, ldb, N, a, stream);
+    }
     if (qout) {
         const gemm::QArgs q{Cq, ldcq, sC, sc_stride_m, sc_stride_nb};
         if (sb_kind == FP8_SB_COL128x1)
@@ -416,7 +562,24 @@ fp8_status_t fp8_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA
                                   int64_t sb_stride_kb, int64_t sb_stride_n, int sb_kind, uint16_t* C, int64_t ldc,
                                   int64_t M, int64_t N, int64_t K, void* stream) {
     return gemm_entry(A, lda, sA, sa_stride_m, sa_stride_kb, B, ldb, sB, sb_stride_kb, sb_stride_n, sb_kind, C, ldc,
-                      nullptr, 0, nullptr, 0, 0, M, N, K, false, as_stream(stream));
+                      nullptr, 0, nullptr, 0, 0, M, N, K, GemmKind::kPromote, as_stream(stream));
+}
+
+fp8_status_t fp8_selftest_gemm_timeout(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                       uint16_t* C, int64_t M, int64_t N, int64_t K, uint64_t wait_ns,
+                                       void* stream) {
+    if (wait_ns < 1000ull || wait_ns > 1000000000ull) return FP8_ERR_ARG;
+    if (K < 256) return FP8_ERR_SHAPE;
+    return gemm_entry(A, K, sA, 1, M, B, K, sB, N / 128, 1, FP8_SB_BLOCK128x128, C, N, nullptr, 0, nullptr, 0, 0, M,
+                      N, K, GemmKind::kPromote, as_stream(stream), wait_ns, 1);
+}
+
+fp8_status_t fp8_gemm_blockscaled_mx(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
+                                     int64_t sa_stride_kb, const uint8_t* B, int64_t ldb, const float* sB,
+                                     int64_t sb_stride_kb, int64_t sb_stride_n, int sb_kind, uint16_t* C, int64_t ldc,
+                                     int64_t M, int64_t N, int64_t K, void* stream) {
+    return gemm_entry(A, lda, sA, sa_stride_m, sa_stride_kb, B, ldb, sB, sb_stride_kb, sb_stride_n, sb_kind, C, ldc,
+                      nullptr, 0, nullptr, 0, 0, M, N, K, GemmKind::kMx, as_stream(stream));
 }
 
 fp8_status_t fp8_gemm_blockscaled_q1x128(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
@@ -425,13 +588,17 @@ fp8_status_t fp8_gemm_blockscaled_q1x128(const uint8_t* A, int64_t lda, const fl
                                          int64_t ldcq, float* sC, int64_t sc_stride_m, int64_t sc_stride_nb,
                                          int64_t M, int64_t N, int64_t K, void* stream) {
     return gemm_entry(A, lda, sA, sa_stride_m, sa_stride_kb, B, ldb, sB, sb_stride_kb, sb_stride_n, sb_kind, nullptr,
-                      0, Cq, ldcq, sC, sc_stride_m, sc_stride_nb, M, N, K, true, as_stream(stream));
+                      0, Cq, ldcq, sC, sc_stride_m, sc_stride_nb, M, N, K, GemmKind::kPromoteQuantOut,
+                      as_stream(stream));
 }
 
-fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
-                                          int64_t sa_stride_kb, const uint8_t* B, const float* sB,
-                                          const int32_t* d_group_offsets, int G, int64_t M_total, int64_t N,
-                                          int64_t K, uint16_t* C, int64_t ldc, void* stream) {
+}  // extern "C"
+
+namespace {
+
+fp8_status_t grouped_entry(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
+                           const uint8_t* B, const float* sB, const int32_t* d_group_offsets, int G, int64_t M_total,
+                           int64_t N, int64_t K, uint16_t* C, int64_t ldc, bool mx, cudaStream_t stream) {
     if (G < 1 || G > gemm::MAX_GROUPS) return FP8_ERR_ARG;
     if (M_total < 0 || N < 0 || K < 0 || M_total % 128 || N % 128 || K % 128) return FP8_ERR_SHAPE;
     if (M_total == 0 || N == 0) return FP8_OK;
@@ -465,8 +632,31 @@ fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda, const f
     a.sb_cols = static_cast<int>(NB);
     a.offsets = d_group_offsets;
     a.G = G;
-    return launch_gemm<gemm::SB_BLOCK, true>(A, lda, M_total, B, K, static_cast<int64_t>(G) * N, a,
-                                             as_stream(stream));
+    a.wait_ns = kWaitTimeoutNs;
+    a.withhold = 0;
+    if (mx)
+        return launch_gemm_mx<gemm::SB_BLOCK, true>(A, lda, M_total, B, K, static_cast<int64_t>(G) * N, a, stream);
+    return launch_gemm<gemm::SB_BLOCK, true>(A, lda, M_total, B, K, static_cast<int64_t>(G) * N, a, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
+                                          int64_t sa_stride_kb, const uint8_t* B, const float* sB,
+                                          const int32_t* d_group_offsets, int G, int64_t M_total, int64_t N,
+                                          int64_t K, uint16_t* C, int64_t ldc, void* stream) {
+    return grouped_entry(A, lda, sA, sa_stride_m, sa_stride_kb, B, sB, d_group_offsets, G, M_total, N, K, C, ldc,
+                         false, as_stream(stream));
+}
+
+fp8_status_t fp8_grouped_gemm_blockscaled_mx(const uint8_t* A, int64_t lda, const float* sA, int64_t sa_stride_m,
+                                             int64_t sa_stride_kb, const uint8_t* B, const float* sB,
+                                             const int32_t* d_group_offsets, int G, int64_t M_total, int64_t N,
+                                             int64_t K, uint16_t* C, int64_t ldc, void* stream) {
+    return grouped_entry(A, lda, sA, sa_stride_m, sa_stride_kb, B, sB, d_group_offsets, G, M_total, N, K, C, ldc,
+                         true, as_stream(stream));
 }
 
 }  // extern "C"

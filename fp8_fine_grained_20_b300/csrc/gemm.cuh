@@ -91,6 +91,8 @@ struct Args {
     int sb_cols;              // number of valid sB columns: N/128 (block) or N (per column)
     const int32_t* offsets;   // grouped only (device)
     int G;
+    uint64_t wait_ns;         // bound of every pipeline wait (kWaitTimeoutNs unless a test shortens it)
+    int withhold;             // test only: the TMA producer stops after the first K-block of its first tile
 };
 
 // Outputs of the quantizing epilogue (a separate kernel parameter, so that
@@ -307,13 +309,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------ TMA producer ----
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
-            bool ok = true, issued_any = false;
-            for (int t = pair; ok && t < num_tiles; t += n_pairs) {
+            bool ok = true, withheld = false;
+            for (int t = pair; ok && !withheld && t < num_tiles; t += n_pairs) {
                 const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
                 const int a_y = tl.row0 + static_cast<int>(rank) * BM;
                 const int b_y = tl.g * p.N + tl.nb * BN + static_cast<int>(rank) * BNH;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait(&done[stage], phase ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&done[stage], phase ^ 1u, abort_flag, p.wait_ns)) {
                         signal_abort(abort_flag, peer);
                         ok = false;
                         break;
@@ -322,15 +324,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(&full[stage], STAGE_TX);
                     tma_load_2d_pair(sm_a + stage * A_BYTES, &tmA, fbar, kb * BK, a_y);
                     tma_load_2d_pair(sm_b + stage * B_BYTES, &tmB, fbar, kb * BK, b_y);
-                    issued_any = true;
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if (p.withhold) {   // test of the failure path: the next K-block never arrives
+                        withheld = true;
+                        break;
+                    }
                 }
             }
-            // after an abort, let the loads still in flight land before the CTA may exit
-            if (!ok && issued_any) spin_ns(100000);
         }
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer ----
@@ -341,8 +344,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     const uint32_t buf = it & 1u;
                     const uint32_t tph = (it >> 1) & 1u;
-                    if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag) ||
-                        !mbar_wait(&full[stage], phase, abort_flag)) {
+                    if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, p.wait_ns) ||
+                        !mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
                         signal_abort(abort_flag, peer);
                         ok = false;
                         break;
@@ -377,7 +380,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int r0 = tl.row0 + static_cast<int>(rank) * BM;
             const float* sb_base = p.sB + static_cast<int64_t>(tl.g) * p.sb_group_stride;
             for (int kb = 0; kb < p.k_blocks; ++kb) {
-                if (!__all_sync(0xffffffffu, mbar_wait(&sempty[slot], sph ^ 1u, abort_flag))) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&sempty[slot], sph ^ 1u, abort_flag, p.wait_ns))) {
                     if (lane == 0) signal_abort(abort_flag, peer);
                     ok = false;
                     break;
@@ -438,8 +441,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t buf = it & 1u;
                 const uint32_t slot = it % SSLOTS, sph = (it / SSLOTS) & 1u;
                 const uint32_t stage = it % STAGES, phase = (it / STAGES) & 1u;
-                const bool ready = mbar_wait(&sfull[slot], sph, abort_flag) &&
-                                   mbar_wait(&done[stage], phase, abort_flag);
+                const bool ready = mbar_wait(&sfull[slot], sph, abort_flag, p.wait_ns) &&
+                                   mbar_wait(&done[stage], phase, abort_flag, p.wait_ns);
                 if (!__all_sync(0xffffffffu, ready)) {  // warp-uniform: tcgen05.ld is .sync.aligned
                     if (lane == 0) signal_abort(abort_flag, peer);
                     ok = false;
@@ -608,9 +611,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     }
 
+    // Teardown.  After the first cluster barrier no thread of either CTA waits
+    // or signals any more (the peer no longer touches this CTA's barriers or
+    // TMEM), and an abort has set the flag of both CTAs; if one happened, the
+    // producers' last TMA loads may still be landing, so both CTAs give them
+    // 100 us before the memory they write is released.
     tc_fence_before_sync();
     __syncthreads();
-    cluster_sync();     // the peer no longer signals this CTA's barriers or reads its TMEM
+    cluster_sync();
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) spin_ns(100000);
+        __syncthreads();
+        cluster_sync();
+    }
     if (warp == 1) {
         tc_fence_after_sync();
         tmem_dealloc_pair(tmem, TMEM_COLS);

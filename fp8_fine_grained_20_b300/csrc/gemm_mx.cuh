@@ -1,0 +1,458 @@
+// gemm_mx.cuh -- block-scaled FP8 GEMM with power-of-two scales applied by the
+// tensor core (tcgen05.mma ... kind::mxf8f6f4.block_scale, UE8M0 scales), for
+// sm_103a.  Same operands and scale layouts as k_gemm_blockscaled, but every
+// scale must be a power of two (the output of the *_pow2 quantizers).
+//
+// Method: the pages' scaling factors for some activations are integral powers
+// of 2 (why-be.why-be.co.kr post 55081; sunipension.com post 314414).  With
+// power-of-two scales the per-group scaling can be done inside the MMA: each
+// 32-deep slice of K carries one 8-bit exponent scale per row of A and per
+// column of B, so C = sum_kb sA[m,kb] sB(kb,n) sum_k A[m,k] B[n,k] is computed
+// entirely by the tensor core, accumulating in FP32 tensor memory (which on
+// this GPU keeps a 24-bit significand over any K), with no FP32 promotion on
+// CUDA cores.  The 128-wide scale groups are replicated over their four
+// 32-deep slices.
+//
+// Scale factors in tensor memory (measured on B300 with an in-bounds layout
+// probe, and the layout the block-scaling section of the PTX ISA describes):
+// for scale_vec::1X the A scale of row m is read from TMEM lane m, column
+// base + m/32, byte sf_id; the B scale of column n from lane 32 (m/32) + n%32
+// (the quadrant of the output row), column base + n/32, byte sf_id.
+// tcgen05.cp .32x128b.warpx4 copies a 512-byte shared-memory atom -- 32
+// chunks of 16 bytes, chunk i holding rows i, i+32, i+64, i+96 as four 32-bit
+// words -- into four TMEM columns of every lane quadrant (lane L receives
+// chunk L % 32), which is exactly that layout.  With a CTA pair, each CTA's
+// TMEM receives its own shared memory's atom and holds the A scales of its own
+// 128 rows and the B scales of all 256 columns.  A 32-bit word has four
+// bytes and sf_id picks one, so one word carries the scales of four
+// consecutive K-blocks: one set of copies serves four K-blocks.
+//
+// Warp roles (384 threads, clusters of 2 CTAs, persistent over 256 x 256 pair
+// tiles in the grouped raster of gemm.cuh):
+//   warp 0 (both CTAs): TMA producer, as in k_gemm_blockscaled, STAGES-deep;
+//   warp 1 (even CTA): MMA issuer -- per group of four K-blocks, three
+//     tcgen05.cp (A atom, two B atoms) into one of SF_SLOTS TMEM scale slots,
+//     then per K-block four block-scaled MMAs (K = 32 each, sf_id = the
+//     K-block's byte) into the single 256-column accumulator and one commit
+//     that frees the smem stage; after the group's last K-block a commit that
+//     frees the scale slot; after the tile's last K-block a commit that hands
+//     the accumulator to the epilogue;
+//   warp 2 (both CTAs): scale loader -- reads the fp32 scales of a group of
+//     four K-blocks, converts them to UE8M0 bytes (the fp32 exponent field;
+//     any non-power-of-two scale sets FP8_ERR_DEVICE_SCALES) and writes the
+//     atoms into a shared-memory slot;
+//   warps 4-11 (both CTAs): epilogue -- load the whole 128 x 256 FP32
+//     accumulator of this CTA into registers (128 values per thread), release
+//     it to the MMA issuer at once, then round to bf16 and store, overlapping
+//     the next tile's MMAs.
+#pragma once
+
+#include "gemm.cuh"
+
+namespace fp8fg {
+namespace gemm {
+
+constexpr int MX_STAGES = 6;
+constexpr int SF_SLOTS = 3;                 // groups of four K-blocks in flight
+constexpr int KB_PER_SF = 4;                // K-blocks per scale word (bytes 0..3)
+constexpr uint32_t SFA_BYTES = 512;         // one atom: 128 rows x 4 bytes
+constexpr uint32_t SFB_BYTES = 1024;        // two atoms: 256 columns x 4 bytes
+constexpr uint32_t SF_TMEM_COL0 = 256;      // the accumulator uses columns 0..255
+constexpr uint32_t SF_TMEM_SLOT = 16;       // A at +0..3, B at +8..15
+constexpr int kStatusBadScale = 9;
+
+constexpr size_t MX_OFF_A = 0;
+constexpr size_t MX_OFF_B = MX_OFF_A + MX_STAGES * A_BYTES;
+constexpr size_t MX_OFF_SFA = MX_OFF_B + MX_STAGES * B_BYTES;
+constexpr size_t MX_OFF_SFB = MX_OFF_SFA + SF_SLOTS * SFA_BYTES;
+constexpr size_t MX_OFF_BAR = MX_OFF_SFB + SF_SLOTS * SFB_BYTES;
+constexpr int MX_N_BARS = 2 * MX_STAGES + 2 * SF_SLOTS + 3;
+constexpr size_t MX_OFF_MISC = MX_OFF_BAR + MX_N_BARS * sizeof(uint64_t);
+constexpr size_t MX_OFF_GOFF = MX_OFF_MISC + 16;
+constexpr size_t MX_SMEM_PLAIN = 1024 + MX_OFF_GOFF;
+constexpr size_t MX_SMEM_GROUPED = 1024 + MX_OFF_GOFF + 2 * (MAX_GROUPS + 1) * sizeof(int);
+static_assert(SF_TMEM_COL0 + SF_SLOTS * SF_TMEM_SLOT <= TMEM_COLS, "tensor memory budget");
+static_assert(MX_SMEM_GROUPED <= 227 * 1024, "shared memory budget");
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4 with E4M3 A and B,
+// both K-major, UE8M0 scales: B scale byte (bits 4-5), A and B formats E4M3 (0),
+// N >> 3 at bits 17-22, scale type UE8M0 (bit 23), M >> 4 at bits 24-28, A
+// scale byte (bits 29-30).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, uint32_t sf_id) {
+    return (sf_id << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(m >> 4) << 24) | (sf_id << 29);
+}
+
+// Shared-memory descriptor of a tcgen05.cp source without swizzling: rows of
+// 16 bytes, 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_sf_atom(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(16u >> 4) << 16;
+    d |= static_cast<uint64_t>(128u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    return d;
+}
+
+__device__ __forceinline__ void tc_cp_sf_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// D[tmem of both CTAs] (+)= (A * sA)[smem] * (B * sB)[smem]^T with the A and B
+// scales read from tensor memory at sfa / sfb; issued by one thread of the
+// even CTA.
+__device__ __forceinline__ void umma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa, uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+
+// UE8M0 byte of a power-of-two fp32 scale: its exponent field (2^-127, the
+// fp32 subnormal 0x00400000, and 0 both give byte 0).  Anything else is not a
+// valid scale for this kernel and is reported.
+__device__ __forceinline__ uint32_t ue8m0_of(float s, bool& bad) {
+    const uint32_t u = __float_as_uint(s);
+    const uint32_t e = u >> 23;
+    bad |= !(((u & 0x7FFFFFu) == 0u && e < 255u) || u == 0x00400000u);
+    return e & 0xFFu;
+}
+
+// Arrive once on an mbarrier of this CTA or the peer with cluster-scope
+// release, so that this thread's earlier shared-memory writes are visible to
+// a tcgen05.cp the peer issues after its acquire.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+__device__ __forceinline__ void sts_u32(void* p, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Acquire-side wait at cluster scope (the releases come from both CTAs).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                                  uint64_t timeout_ns) {
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
+        if (mbar_try_wait_cluster(a, parity)) return true;
+        if ((i & 31u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+    return false;
+}
+
+// Launch: clusters of 2 CTAs along x, THREADS threads, MX_SMEM_PLAIN or
+// MX_SMEM_GROUPED bytes of dynamic shared memory, one CTA per SM.
+template <int SBK, bool GROUPED>
+__global__ void __launch_bounds__(THREADS, 1)
+    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sm_a = base + MX_OFF_A;
+    uint8_t* sm_b = base + MX_OFF_B;
+    uint8_t* sm_sfa = base + MX_OFF_SFA;
+    uint8_t* sm_sfb = base + MX_OFF_SFB;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + MX_OFF_BAR);
+    uint64_t* full = bars;                   // even CTA: TMA bytes of both CTAs
+    uint64_t* done = full + MX_STAGES;       // both: the stage's MMAs completed (stage free)
+    uint64_t* sfull = done + MX_STAGES;      // even CTA: both CTAs' scale atoms of a slot written
+    uint64_t* sfdone = sfull + SF_SLOTS;     // both: the slot's copies and MMAs completed
+    uint64_t* accfull = sfdone + SF_SLOTS;   // both: the tile's accumulator is complete
+    uint64_t* accempty = accfull + 1;        // even CTA: both CTAs' epilogues hold the accumulator
+    uint64_t* drain = accempty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + MX_OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(base + MX_OFF_MISC + 4);
+    int* groups_ok = reinterpret_cast<int*>(base + MX_OFF_MISC + 8);
+    int* goff = reinterpret_cast<int*>(base + MX_OFF_GOFF);
+    int* ppre = goff + (MAX_GROUPS + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < MX_STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&done[i], 1);
+        }
+        for (int i = 0; i < SF_SLOTS; ++i) {
+            mbar_init(&sfull[i], 2);
+            mbar_init(&sfdone[i], 1);
+        }
+        mbar_init(accfull, 1);
+        mbar_init(accempty, 2 * PROMO_WARPS);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        *groups_ok = 1;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (GROUPED) {
+        for (int i = threadIdx.x; i <= p.G; i += THREADS) goff[i] = p.offsets[i];
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    __syncthreads();
+    if (GROUPED && threadIdx.x == 0) {
+        bool ok = goff[0] >= 0 && goff[p.G] <= p.M && (goff[p.G] % BM) == 0;
+        int acc = 0;
+        for (int g = 0; g < p.G; ++g) {
+            ok = ok && goff[g] <= goff[g + 1] && (goff[g] % BM) == 0;
+            ppre[g] = acc;
+            if (ok) acc += (goff[g + 1] - goff[g] + PM - 1) / PM;
+        }
+        ppre[p.G] = acc;
+        if (!ok) {
+            *groups_ok = 0;
+            if (blockIdx.x == 0) record_status(kStatusBadGroups);
+        }
+    }
+    tc_fence_before_sync();
+    cluster_sync();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int pair_rows = GROUPED ? ppre[p.G] : (p.m_blocks + 1) / 2;
+    const int num_tiles = (*groups_ok) ? pair_rows * p.n_blocks : 0;
+    const int pair = static_cast<int>(cluster_id_x());
+    const int n_pairs = static_cast<int>(n_clusters_x());
+    const int groups_per_tile = (p.k_blocks + KB_PER_SF - 1) / KB_PER_SF;
+
+    // register split: 4 warps x 80 + 8 warps x 208 = 63,488 <= 384 x 168 launched
+    if (warp < 4) {
+      regs_decrease<80>();
+      if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < num_tiles; t += n_pairs) {
+                const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+                const int a_y = tl.row0 + static_cast<int>(rank) * BM;
+                const int b_y = tl.g * p.N + tl.nb * BN + static_cast<int>(rank) * BNH;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&done[stage], phase ^ 1u, abort_flag, p.wait_ns)) {
+                        signal_abort(abort_flag, peer);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fbar = mapa_shared(smem_addr(&full[stage]), 0);
+                    if (leader) mbar_arrive_expect_tx(&full[stage], STAGE_TX);
+                    tma_load_2d_pair(sm_a + stage * A_BYTES, &tmA, fbar, kb * BK, a_y);
+                    tma_load_2d_pair(sm_b + stage * B_BYTES, &tmB, fbar, kb * BK, b_y);
+                    if (++stage == MX_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // -------------------------------------------------- MMA issuer ----
+        if (leader && lane == 0) {
+            uint32_t stage = 0, phase = 0, grp = 0, tile_it = 0;
+            bool ok = true;
+            for (int t = pair; ok && t < num_tiles; t += n_pairs, ++tile_it) {
+                for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
+                    const uint32_t sslot = grp % SF_SLOTS, sph = (grp / SF_SLOTS) & 1u;
+                    const uint32_t sfa_t = tmem + SF_TMEM_COL0 + sslot * SF_TMEM_SLOT;
+                    const uint32_t sfb_t = sfa_t + 8;
+                    const uint32_t j = static_cast<uint32_t>(kb % KB_PER_SF);
+                    if (j == 0) {
+                        // a new group: its scale atoms are in shared memory and the TMEM
+                        // slot's previous group has finished its MMAs
+                        if (!mbar_wait_cluster(&sfull[sslot], sph, abort_flag, p.wait_ns) ||
+                            !mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns)) {
+                            signal_abort(abort_flag, peer);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        tc_cp_sf_pair(sfa_t, sdesc_sf_atom(smem_addr(sm_sfa + sslot * SFA_BYTES)));
+                        tc_cp_sf_pair(sfb_t, sdesc_sf_atom(smem_addr(sm_sfb + sslot * SFB_BYTES)));
+                        tc_cp_sf_pair(sfb_t + 4, sdesc_sf_atom(smem_addr(sm_sfb + sslot * SFB_BYTES + 512)));
+                    }
+                    if (kb == 0 && !mbar_wait(accempty, (tile_it & 1u) ^ 1u, abort_flag, p.wait_ns)) {
+                        signal_abort(abort_flag, peer);
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
+                        signal_abort(abort_flag, peer);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t ad = sdesc_kmajor_sw128(smem_addr(sm_a + stage * A_BYTES));
+                    const uint64_t bd = sdesc_kmajor_sw128(smem_addr(sm_b + stage * B_BYTES));
+                    const uint32_t idesc = idesc_mx_e4m3(PM, BN, j);
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        umma_mx_pair(tmem, ad + 2u * k, bd + 2u * k, idesc, sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
+                    umma_commit_pair_mc(&done[stage], 0x3);
+                    if (j == KB_PER_SF - 1 || kb == p.k_blocks - 1) {
+                        umma_commit_pair_mc(&sfdone[sslot], 0x3);
+                        ++grp;
+                    }
+                    if (kb == p.k_blocks - 1) umma_commit_pair_mc(accfull, 0x3);
+                    if (++stage == MX_STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every copy and MMA this thread issued completes before TMEM is released
+            umma_commit_pair_mc(drain, 0x1);
+            mbar_wait(drain, 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------ scale loader ----
+        uint32_t grp = 0;
+        bool ok = true, bad = false;
+        const uint32_t sfull_even = mapa_shared(smem_addr(&sfull[0]), 0);
+        for (int t = pair; ok && t < num_tiles; t += n_pairs) {
+            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            const int r0 = tl.row0 + static_cast<int>(rank) * BM;
+            const float* sb_base = p.sB + static_cast<int64_t>(tl.g) * p.sb_group_stride;
+            for (int gi = 0; gi < groups_per_tile; ++gi, ++grp) {
+                const uint32_t sslot = grp % SF_SLOTS, sph = (grp / SF_SLOTS) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns))) {
+                    if (lane == 0) signal_abort(abort_flag, peer);
+                    ok = false;
+                    break;
+                }
+                const int kb0 = gi * KB_PER_SF;
+                const int nk = min(KB_PER_SF, p.k_blocks - kb0);
+                // A atom: word i of this lane's 16-byte chunk is row lane + 32 i of this
+                // CTA's half; byte b of a word is K-block kb0 + b
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+                    const int row = r0 + lane + 32 * i;
+                    const float* src = p.sA + static_cast<int64_t>(row) * p.sa_sm + static_cast<int64_t>(kb0) * p.sa_skb;
+                    uint32_t w = 0;
+#pragma unroll
+                    for (int b = 0; b < KB_PER_SF; ++b) {
+                        const float sv = (row < p.M && b < nk) ? src[static_cast<int64_t>(b) * p.sa_skb] : 0.0f;
+                        w |= ue8m0_of(sv, bad) << (8 * b);
+                    }
+                    sts_u32(sm_sfa + sslot * SFA_BYTES + 16 * lane + 4 * i, w);
+                }
+                // B atoms: atom h covers tile columns 128 h .. 128 h + 127 (word i of the
+                // chunk: column 128 h + lane + 32 i); block scales fill an atom with one word
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll 1
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = (SBK == SB_BLOCK) ? tl.nb * (BN / 128) + h : tl.nb * BN + 128 * h + lane + 32 * i;
+                        const float* src = sb_base + static_cast<int64_t>(kb0) * p.sb_skb + static_cast<int64_t>(c) * p.sb_sn;
+                        uint32_t w = 0;
+#pragma unroll
+                        for (int b = 0; b < KB_PER_SF; ++b) {
+                            const float sv = (c < p.sb_cols && b < nk) ? src[static_cast<int64_t>(b) * p.sb_skb] : 0.0f;
+                            w |= ue8m0_of(sv, bad) << (8 * b);
+                        }
+                        sts_u32(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane + 4 * i, w);
+                    }
+                }
+                fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_release(sfull_even + sslot * sizeof(uint64_t));
+            }
+        }
+        if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(kStatusBadScale);
+      }
+    } else {
+        regs_increase<208>();
+        // ------------------------------------------------------ epilogue ----
+        const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
+        const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
+        const int row = quarter * 32 + lane;
+        uint32_t tile_it = 0;
+        for (int t = pair; t < num_tiles; t += n_pairs, ++tile_it) {
+            if (!__all_sync(0xffffffffu, mbar_wait(accfull, tile_it & 1u, abort_flag, p.wait_ns))) {
+                if (lane == 0) signal_abort(abort_flag, peer);
+                break;
+            }
+            tc_fence_after_sync();
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * 128;
+            uint32_t r0[32], r1[32], r2[32], r3[32];
+            tmem_ld_32cols(taddr + 0, r0);
+            tmem_ld_32cols(taddr + 32, r1);
+            tmem_wait_ld2(r0, r1);
+            tmem_ld_32cols(taddr + 64, r2);
+            tmem_ld_32cols(taddr + 96, r3);
+            tmem_wait_ld2(r2, r3);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(accempty), 0));   // the even CTA's
+            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
+            const int n0 = tl.nb * BN + half * 128;
+            if (!(grow < tl.row_end && n0 < p.N)) continue;
+            uint16_t* crow = p.C + static_cast<int64_t>(grow) * p.ldc + n0;
+            auto store32 = [&](const uint32_t (&r)[32], int c0) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
+                    stg_v4(crow + c0 + 8 * j, w);
+                }
+            };
+            store32(r0, 0);
+            store32(r1, 32);
+            store32(r2, 64);
+            store32(r3, 96);
+        }
+    }
+
+    // Teardown.  After the first cluster barrier no thread of either CTA waits
+    // or signals any more, and an abort has set the flag of both CTAs; if one
+    // happened, the producers' last TMA loads may still be landing, so both
+    // CTAs give them 100 us before the memory they write is released.
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync();
+    if (*abort_flag) {
+        if (warp == 0 && lane == 0) spin_ns(100000);
+        __syncthreads();
+        cluster_sync();
+    }
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm
+}  // namespace fp8fg

@@ -51,6 +51,28 @@ __device__ __forceinline__ GroupScale group_scale(float amax) {
     return g;
 }
 
+// Power-of-two scale of a group: amax = m 2^E (m in [1, 2)) needs 448 2^e =
+// 1.75 2^(e+8) >= amax, so e = E - 8 when m <= 1.75 and E - 7 otherwise;
+// subnormal amax and anything below clamp to e = -127, whose scale 2^-127 is
+// itself an fp32 subnormal (bit pattern 0x00400000).  r = 2^-e is exact.
+__device__ __forceinline__ GroupScale group_scale_pow2(float amax) {
+    GroupScale g;
+    const uint32_t u = __float_as_uint(amax);
+    const int eb = static_cast<int>(u >> 23);
+    int e = eb - 135 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    if (eb == 0 || e < -127) e = -127;
+    g.s = (e >= -126) ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+    g.r = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+    g.mode = (amax == 0.0f) ? 0 : 1;
+    if (amax == 0.0f) g.s = 0.0f;
+    return g;
+}
+
+template <bool POW2>
+__device__ __forceinline__ GroupScale group_scale_t(float amax) {
+    return POW2 ? group_scale_pow2(amax) : group_scale(amax);
+}
+
 // RN(x / s) for a pair of values by Markstein's two-step correction; r2 =
 // (RN(1/s0), RN(1/s1)), ns2 = (-s0, -s1).
 __device__ __forceinline__ float2 div2_markstein(float2 x, float2 r2, float2 ns2) {
@@ -96,15 +118,24 @@ __device__ __forceinline__ uint32_t quant_div(float x, float s, int mode) {
     return c | ((__float_as_uint(x) >> 24) & 0x80u);
 }
 
+// RN(x / s) of a pair: Markstein's correction, or one multiply by r = 1/s
+// when s is a power of two (then x r is the exact quotient, rounded once).
+template <bool POW2>
+__device__ __forceinline__ float2 div2_t(float2 x, float2 r2, float2 ns2) {
+    if (POW2) return __fmul2_rn(x, r2);
+    return div2_markstein(x, r2, ns2);
+}
+
 // Eight codes of eight bf16 values (one 16-byte chunk) of one group.
+template <bool POW2 = false>
 __device__ __forceinline__ uint2 quant8_bf16(const uint4& v, const GroupScale& g) {
     if (g.mode == 1) {
         const float2 r2 = make_float2(g.r, g.r);
         const float2 ns2 = make_float2(-g.s, -g.s);
-        const uint32_t c0 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.x), r2, ns2));
-        const uint32_t c1 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.y), r2, ns2));
-        const uint32_t c2 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.z), r2, ns2));
-        const uint32_t c3 = e4m3_pair(div2_markstein(bf16x2_to_f32x2(v.w), r2, ns2));
+        const uint32_t c0 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.x), r2, ns2));
+        const uint32_t c1 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.y), r2, ns2));
+        const uint32_t c2 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.z), r2, ns2));
+        const uint32_t c3 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.w), r2, ns2));
         // sign bits (bit 15 of each bf16) into bit 7 of each code byte
         const uint32_t sx = __byte_perm(v.x, v.y, 0x7531) & 0x80808080u;
         const uint32_t sy = __byte_perm(v.z, v.w, 0x7531) & 0x80808080u;
@@ -177,7 +208,7 @@ __device__ __forceinline__ void sts_v4(void* p, uint4 v) {
 // per slot and each lane quantizes 32 values with one scale computation.
 // UNROLL slots per iteration keep 4*UNROLL 16-byte loads in flight per lane;
 // grid-stride over slots in row-major group order.
-template <int UNROLL>
+template <int UNROLL, bool POW2 = false>
 __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restrict__ x, int M, int KB,
                                                          int64_t ldx, uint8_t* __restrict__ q, int64_t ldq,
                                                          float* __restrict__ s, int64_t ssm, int64_t sskb) {
@@ -222,10 +253,10 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
             a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
             if (mu[u] < M) {
-                const GroupScale g = group_scale(a);
+                const GroupScale g = group_scale_t<POW2>(a);
                 uint8_t* dst = q + static_cast<int64_t>(mu[u]) * ldq + kbu[u] * 128 + sub * 8;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) stg_v2(dst + 32 * i, quant8_bf16(v[u][i], g));
+                for (int i = 0; i < 4; ++i) stg_v2(dst + 32 * i, quant8_bf16<POW2>(v[u][i], g));
                 if (sub == 0) s[static_cast<int64_t>(mu[u]) * ssm + static_cast<int64_t>(kbu[u]) * sskb] = g.s;
             }
         }
@@ -276,6 +307,7 @@ __device__ __forceinline__ uint32_t lds_u32(const void* p) {
     return v;
 }
 
+template <bool POW2 = false>
 __global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_constant__ CUtensorMap tmW,
                                                                    const QuantWArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -346,14 +378,14 @@ __global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_
         am = red[0];
 #pragma unroll
         for (int k = 1; k < 8; ++k) am = fmaxf(am, red[k]);
-        const GroupScale gs = group_scale(am);
+        const GroupScale gs = group_scale_t<POW2>(am);
         if (tid == 0)
             a.s[static_cast<int64_t>(g) * a.s_gstride + static_cast<int64_t>(kb) * a.sskb +
                 static_cast<int64_t>(nb) * a.ssnb] = gs.s;
 
         uint2 rows[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) rows[j] = quant8_bf16(v[j], gs);
+        for (int j = 0; j < 8; ++j) rows[j] = quant8_bf16<POW2>(v[j], gs);
         uint8_t* qg = a.q + static_cast<int64_t>(g) * a.q_gstride;
         if (!a.kmajor) {
 #pragma unroll
@@ -433,6 +465,7 @@ __device__ __forceinline__ void sts_u16(void* p, uint32_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_addr(p)), "h"(static_cast<uint16_t>(v)) : "memory");
 }
 
+template <bool POW2 = false>
 __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const __grid_constant__ CUtensorMap tmQ,
                                                                           const RequantArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -540,7 +573,7 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
         am0 = fmaxf(am0, __shfl_xor_sync(0xffffffffu, am0, 16));
         am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 8));
         am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 16));
-        const GroupScale gs = group_scale((g & 1) ? am1 : am0);   // lane (g, c): channel 2c + (g & 1)
+        const GroupScale gs = group_scale_t<POW2>((g & 1) ? am1 : am0);   // lane (g, c): channel 2c + (g & 1)
         if (g < 2)
             a.sT[static_cast<int64_t>(kb * 128 + 16 * w + 2 * c + g) * a.sTk + static_cast<int64_t>(mb) * a.sTmb] =
                 gs.s;
@@ -562,7 +595,7 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
                 const float2 ns2 = make_float2(-chs[j], -chs[j]);
 #pragma unroll
                 for (int aa = 0; aa < 16; ++aa) {
-                    const uint32_t code = e4m3_pair(div2_markstein(make_float2(xv[aa][j], xv[aa][2 + j]), r2, ns2));
+                    const uint32_t code = e4m3_pair(div2_t<POW2>(make_float2(xv[aa][j], xv[aa][2 + j]), r2, ns2));
                     // sign bits of the two dequantized values: bit 7 of their top bytes
                     const uint32_t top =
                         __byte_perm(__float_as_uint(xv[aa][j]), __float_as_uint(xv[aa][2 + j]), 0x0073);

@@ -64,7 +64,8 @@ typedef enum fp8_status {
     FP8_ERR_DEVICE_TIMEOUT = 5,  /* (device status) a bounded device wait gave up */
     FP8_ERR_ARG = 6,             /* an enum or stride argument is invalid */
     FP8_ERR_DEVICE = 7,          /* the current device is not sm_103 / lacks resources */
-    FP8_ERR_DEVICE_GROUPS = 8    /* (device status) group offsets were not valid */
+    FP8_ERR_DEVICE_GROUPS = 8,   /* (device status) group offsets were not valid */
+    FP8_ERR_DEVICE_SCALES = 9    /* (device status) a scale given to an _mx GEMM is not a power of two */
 } fp8_status_t;
 
 /* Layout of the codes written by fp8_quant_w_128x128. */
@@ -141,6 +142,66 @@ fp8_status_t fp8_requant_1x128_to_128x1(const uint8_t* q, int64_t M, int64_t K, 
                                         void* stream);
 
 /*
+ * SwiGLU recompute fused with 1x128 quantization (why-be.why-be.co.kr, board
+ * post 65900: the inputs of the SwiGLU operator are cached and its output is
+ * recomputed; sunipension.com post 314414, Figure 7(a): 1x128 activation
+ * tiles).  For m < M, f < F:
+ *   y[m][f] = bf16( silu(g) * u ),  silu(g) = g / (1 + e^-g),
+ * with g = gate[m*ldg + f] and u = up[m*ldu + f] (bf16), evaluated in fp32 and
+ * rounded once to bf16 (within one bf16 ulp of the correctly rounded value
+ * while |g| <= 87); then y is 1x128-quantized exactly as fp8_quant_act_1x128
+ * quantizes a bf16 tensor:
+ *   q   E4M3 codes [M][F], row stride ldq (>= F, multiple of 16)
+ *   s   fp32 scales, logical [M][F/128]; (m, fb) at s[m*s_stride_m + fb*s_stride_fb]
+ *   y   optional bf16 [M][F] output of the rounded SwiGLU values (NULL: not written),
+ *       row stride ldy
+ * A fused gate/up projection output [M][2F] is passed as gate = base,
+ * up = base + F, ldg = ldu = 2F.  Requires F % 128 == 0; M may be any value >= 0.
+ */
+fp8_status_t fp8_swiglu_quant_1x128(const uint16_t* gate, int64_t ldg, const uint16_t* up, int64_t ldu,
+                                    int64_t M, int64_t F,
+                                    uint8_t* q, int64_t ldq,
+                                    float* s, int64_t s_stride_m, int64_t s_stride_fb,
+                                    uint16_t* y, int64_t ldy,
+                                    void* stream);
+
+/*
+ * Power-of-two scale variants of the three quantizers (why-be.why-be.co.kr,
+ * board post 55081, and sunipension.com, board post 314414: the scaling
+ * factors of the inputs of the Linear after attention, and of the gradients
+ * before the MoE down-projection, are integral powers of 2).  Each group's
+ * scale is the smallest power of two s = 2^e with amax / s <= 448, never below
+ * 2^-127 (the smallest scale an 8-bit exponent can hold; fp32 bit pattern
+ * 0x00400000); a zero group keeps s = 0 and codes 0x00.  The codes are the E4M3
+ * round-to-nearest-even of x / s, which is exact (one multiply by 2^-e).  The
+ * scales are written as fp32 values; these are the operands of
+ * fp8_gemm_blockscaled_mx.  Arguments, layouts, requirements and status codes
+ * are those of the call without the suffix.  The requantizer expects 1x128
+ * inputs made with power-of-two scales (its dequantizing multiply is then
+ * exact); it accepts any scales and applies the power-of-two rule to the
+ * 128x1 groups.
+ */
+fp8_status_t fp8_quant_act_1x128_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                                      uint8_t* q, int64_t ldq,
+                                      float* s, int64_t s_stride_m, int64_t s_stride_kb,
+                                      void* stream);
+fp8_status_t fp8_quant_w_128x128_pow2(const uint16_t* w, int64_t K, int64_t N, int64_t ldw,
+                                      uint8_t* q, int64_t ldq, int q_layout,
+                                      float* s, int64_t s_stride_kb, int64_t s_stride_nb,
+                                      void* stream);
+fp8_status_t fp8_quant_w_128x128_batched_pow2(const uint16_t* w, int64_t G, int64_t K, int64_t N, int64_t ldw,
+                                              int64_t w_batch_stride,
+                                              uint8_t* q, int64_t ldq, int64_t q_batch_stride, int q_layout,
+                                              float* s, int64_t s_stride_kb, int64_t s_stride_nb,
+                                              int64_t s_batch_stride,
+                                              void* stream);
+fp8_status_t fp8_requant_1x128_to_128x1_pow2(const uint8_t* q, int64_t M, int64_t K, int64_t ldq,
+                                             const float* s, int64_t s_stride_m, int64_t s_stride_kb,
+                                             uint8_t* qT, int64_t ldqT,
+                                             float* sT, int64_t sT_stride_k, int64_t sT_stride_mb,
+                                             void* stream);
+
+/*
  * Block-scaled FP8 GEMM with FP32 promotion every 128 K (Figure 7(b)):
  *   C[m][n] = bf16( sum_kb sA[m,kb] * sB(kb,n) * sum_{k in kb} A[m][k] * B[n][k] )
  * with the inner sums on tcgen05 tensor cores and the outer sum in FP32.
@@ -210,6 +271,42 @@ fp8_status_t fp8_grouped_gemm_blockscaled(const uint8_t* A, int64_t lda,
                                           void* stream);
 
 /*
+ * Block-scaled FP8 GEMM with power-of-two scales applied by the tensor core
+ * (why-be.why-be.co.kr post 55081 and sunipension.com post 314414: scaling
+ * factors that are integral powers of 2).  Computes the same
+ *   C[m][n] = bf16( sum_kb sA[m,kb] * sB(kb,n) * sum_{k in kb} A[m][k] * B[n][k] )
+ * as fp8_gemm_blockscaled, with the same arguments, layouts, requirements and
+ * status codes, but every scale must be a power of two in [2^-127, 2^127] or
+ * zero (the fp32 output of the _pow2 quantizers): each 128-wide group's scale
+ * becomes an 8-bit exponent (UE8M0) for its four 32-deep slices of K, and the
+ * tensor core applies it inside the MMA (tcgen05.mma ... kind::mxf8f6f4
+ * .block_scale), accumulating the whole K in FP32 tensor memory with no FP32
+ * promotion on CUDA cores.  A scale that is not a power of two is used with
+ * its exponent field alone and sets FP8_ERR_DEVICE_SCALES in the device status.
+ */
+fp8_status_t fp8_gemm_blockscaled_mx(const uint8_t* A, int64_t lda,
+                                     const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
+                                     const uint8_t* B, int64_t ldb,
+                                     const float* sB, int64_t sb_stride_kb, int64_t sb_stride_n,
+                                     int sb_kind,
+                                     uint16_t* C, int64_t ldc,
+                                     int64_t M, int64_t N, int64_t K,
+                                     void* stream);
+
+/*
+ * fp8_grouped_gemm_blockscaled with power-of-two scales applied by the tensor
+ * core, as fp8_gemm_blockscaled_mx does; arguments, layouts, requirements and
+ * status codes are those of fp8_grouped_gemm_blockscaled.
+ */
+fp8_status_t fp8_grouped_gemm_blockscaled_mx(const uint8_t* A, int64_t lda,
+                                             const float* sA, int64_t sa_stride_m, int64_t sa_stride_kb,
+                                             const uint8_t* B, const float* sB,
+                                             const int32_t* d_group_offsets, int G,
+                                             int64_t M_total, int64_t N, int64_t K,
+                                             uint16_t* C, int64_t ldc,
+                                             void* stream);
+
+/*
  * Tensor-core accumulation probe (why-be.why-be.co.kr post 55081: the
  * previous generation's FP8 tensor cores keep about 14 bits when they
  * accumulate, hence the promotion every 128 K).  Computes
@@ -231,6 +328,21 @@ fp8_status_t fp8_mma_accumulation_probe(const uint8_t* A, const uint8_t* B, int6
  * with fp8_get_device_status().  FP8_ERR_ARG for a timeout outside the range.
  */
 fp8_status_t fp8_selftest_bounded_wait(uint64_t timeout_ns, void* stream);
+
+/*
+ * Self-test of the GEMM's failure path (no counterpart on the pages).  Runs
+ * fp8_gemm_blockscaled (block scales) on dense operands -- A [M][K], sA
+ * MN-major (sA[kb*M + m]), B [N][K], sB [K/128][N/128], C [M][N] -- with every
+ * pipeline wait bounded by wait_ns (1 us .. 1 s) and the TMA producer
+ * withholding every K-block after the first, so that a wait of the MMA issuer
+ * runs out.  The kernel then records FP8_ERR_DEVICE_TIMEOUT, stops both CTAs
+ * of every pair, lets the loads and MMAs it issued complete, frees its tensor
+ * memory and returns; C is left undefined and the context stays usable.
+ * Requires K >= 256 and the shapes of fp8_gemm_blockscaled.
+ */
+fp8_status_t fp8_selftest_gemm_timeout(const uint8_t* A, const float* sA, const uint8_t* B, const float* sB,
+                                       uint16_t* C, int64_t M, int64_t N, int64_t K, uint64_t wait_ns,
+                                       void* stream);
 
 /*
  * Device status word.  Waits for `stream`, copies the status word of the

@@ -164,3 +164,71 @@ def test_probe_and_selftest_rejections(lib):
     wait = lib.fp8_selftest_bounded_wait
     assert wait(0, NULL) == 6
     assert wait(2_000_000_000, NULL) == 6
+
+
+def test_pow2_quantizer_rejections(lib):
+    f = lib.fp8_quant_act_1x128_pow2
+    assert f(A16, 4, 100, 100, A16b, 100, A16, 1, 4, NULL) == 3            # K % 128
+    assert f(NULL, 4, 128, 128, A16b, 128, A16, 1, 4, NULL) == 1
+    assert f(MIS, 4, 128, 128, A16b, 128, A16, 1, 4, NULL) == 2
+    assert f(A16, 0, 128, 128, A16b, 128, A16, 1, 4, NULL) == 0            # empty
+    w = lib.fp8_quant_w_128x128_pow2
+    assert w(A16, 256, 200, 200, A16b, 256, 0, A16, 2, 1, NULL) == 3
+    assert w(A16, 256, 256, 256, A16b, 256, 7, A16, 2, 1, NULL) == 6
+    wb = lib.fp8_quant_w_128x128_batched_pow2
+    assert wb(A16, 2, 256, 384, 384, 256 * 384 - 8, A16b, 256, 384 * 256, 0, A16, 3, 1, 6, NULL) == 6
+    r = lib.fp8_requant_1x128_to_128x1_pow2
+    assert r(A16, 200, 128, 128, A16, 1, 200, A16b, 200, A16, 1, 128, NULL) == 3
+    assert r(A16, 256, 128, 128, NULL, 1, 256, A16b, 256, A16, 1, 128, NULL) == 1
+
+
+def test_mx_gemm_rejections(lib):
+    f = lib.fp8_gemm_blockscaled_mx
+    ok = [A16, 256, A16, 1, 256, A16b, 256, A16, 2, 1, 0, A16b, 256, 256, 256, 256, NULL]
+    bad = list(ok); bad[10] = 5
+    assert f(*bad) == 6                                   # sb_kind
+    bad = list(ok); bad[14] = 200
+    assert f(*bad) == 3                                   # N % 128
+    bad = list(ok); bad[15] = 0
+    assert f(*bad) == 3                                   # K == 0 with a non-empty output
+    bad = list(ok); bad[11] = NULL
+    assert f(*bad) == 1
+    bad = list(ok); bad[12] = 100
+    assert f(*bad) == 6                                   # ldc < N
+    g = lib.fp8_grouped_gemm_blockscaled_mx
+    ok = [A16, 256, A16, 1, 256, A16b, A16, A16, 4, 256, 256, 256, A16b, 256, NULL]
+    bad = list(ok); bad[8] = 0
+    assert g(*bad) == 6
+    bad = list(ok); bad[7] = NULL
+    assert g(*bad) == 1
+    bad = list(ok); bad[11] = 100
+    assert g(*bad) == 3
+
+
+def test_gemm_timeout_selftest_rejections(lib):
+    f = lib.fp8_selftest_gemm_timeout
+    assert f(A16, A16, A16b, A16, A16b, 128, 256, 256, 10, NULL) == 6          # bound below 1 us
+    assert f(A16, A16, A16b, A16, A16b, 128, 256, 256, 2_000_000_000, NULL) == 6
+    assert f(A16, A16, A16b, A16, A16b, 128, 256, 128, 2_000_000, NULL) == 3   # K < 256
+    assert f(NULL, A16, A16b, A16, A16b, 128, 256, 256, 2_000_000, NULL) == 1
+
+
+def test_swiglu_quant_rejections(lib):
+    f = lib.fp8_swiglu_quant_1x128
+    ok = [A16, 512, A16b, 512, 4, 256, A16, 256, A16b, 1, 4, NULL, 0, NULL]
+    bad = list(ok); bad[5] = 200
+    assert f(*bad) == 3                                   # F % 128
+    bad = list(ok); bad[4] = -1
+    assert f(*bad) == 3
+    bad = list(ok); bad[4] = 0
+    assert f(*bad) == 0                                   # empty: nothing launched
+    bad = list(ok); bad[2] = NULL
+    assert f(*bad) == 1                                   # up
+    bad = list(ok); bad[1] = 128
+    assert f(*bad) == 6                                   # ldg < F
+    bad = list(ok); bad[0] = MIS
+    assert f(*bad) == 2
+    bad = list(ok); bad[11] = A16; bad[12] = 100
+    assert f(*bad) == 6                                   # ldy < F with a y output
+    bad = list(ok); bad[11] = MIS; bad[12] = 256
+    assert f(*bad) == 2                                   # misaligned y
