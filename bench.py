@@ -14,10 +14,17 @@ FP8 training step of a large MoE transformer layer:
                                       x1000 -> 1x128 quantize (dY quantized above);
                                       cached Xwq and dYq -> 1x128 -> 128x1 requantize;
                                       dW = GEMM (128x1 x 128x1 scales) bf16 [7168, 18432]
+  SwiGLU recompute of that MLP        cached gate/up bf16 [8192, 2 x 18432] -> silu(g) u, rounded
+                                      to bf16 and 1x128-quantized in one pass -> codes [8192, 18432]
   MoE expert forward                  16384 tokens x 8 picks (Zipf 1.1 over 32 experts,
                                       padded to 128 rows) bf16 [~133k, 7168] -> 1x128 quantize;
                                       32 experts W_g [7168, 2048] -> 128x128 quantize;
                                       grouped GEMM -> bf16 [~133k, 2048]
+
+`pow2_mx` repeats the step with power-of-two scales: the *_pow2 quantizers and
+the GEMMs whose scales the tensor core applies (no FP32 promotion), timed the
+same way, with the error of both paths against the exact product of the
+original bf16 inputs on sampled outputs.
 
 `value` is the step's GEMM work (2MNK summed over the four GEMMs, routed rows
 for the MoE) divided by the step time, summed over ranks: whole-step TFLOP/s,
@@ -69,6 +76,7 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    p.add_argument("--no-pow2", action="store_true", help="skip the power-of-two / hardware-scaled leg")
     p.add_argument("--steady-seconds", type=float, default=2.0,
                    help="length of the steady-state leg (clock record under sustained load; 0 skips it)")
     return p.parse_args()
@@ -85,6 +93,7 @@ class Workload:
         self.w = synth.weight(2 + s, CIN, COUT)                         # N(0, 0.02^2)
         self.dy = synth.wgrad_tensor(4 + s, 1, T, COUT)                 # N(0,1e-3^2), 0.1% x1000
         self.xw = synth.wgrad_tensor(4 + s, 0, T, CIN)                  # the weight gradient's X, same recipe
+        self.gate_up = synth.swiglu_inputs(6 + s, T, COUT)              # cached gate | up, N(0, 1.7^2)
         moe = synth.moe_inputs(seed=5 + s, G=G, K=MOE_K, N=MOE_N, tokens=TOKENS, topk=TOPK, zipf_s=ZIPF)
         self.moe_x = moe.x
         self.moe_w = moe.w
@@ -113,6 +122,7 @@ class Workload:
             "quant_w_rowmajor": q(CIN, COUT) - CIN * COUT // 128 * 4 + (CIN // 128) * (COUT // 128) * 4,
             "quant_act_dy": q(T, COUT),
             "quant_act_xw": q(T, CIN),
+            "swiglu_quant": T * 2 * COUT * 2 + T * COUT + T * COUT // 128 * 4,
             "requant_x": rq(T, CIN),
             "requant_dy": rq(T, COUT),
             "quant_act_moe": q(self.moe_rows, MOE_K),
@@ -136,6 +146,7 @@ class Workload:
                           "[8192x18432]" % self.moe_rows,
             "wgrad_inputs": "X [8192x7168] and dY [8192x18432] ~ N(0, 1e-3^2) with Bernoulli(0.001) "
                             "elements x1000, each 1x128-quantized then requantized 128x1 along tokens",
+            "swiglu": "cached gate/up [8192, 2x18432] ~ N(0, 1.7^2) -> 1x128 codes [8192, 18432]",
             "l2": "inputs larger than L2 (126 MB); %.1f GB of quantizer traffic per step"
                   % (sum(self.quant_bytes().values()) / 1e9),
             "global_batch": T,
@@ -149,9 +160,9 @@ class DeviceStep:
     """Device buffers and the sequence of library calls of one step."""
 
     KERNELS = ["quant_act_x", "quant_w", "gemm_fprop", "quant_act_dy", "quant_w_rowmajor", "gemm_dgrad",
-               "quant_act_xw", "requant_x", "requant_dy", "gemm_wgrad", "quant_act_moe", "quant_w_moe",
-               "grouped_gemm_moe"]
-    LAUNCHES_PER_STEP = 13      # the 32 expert weights are quantized in one batched launch
+               "swiglu_quant", "quant_act_xw", "requant_x", "requant_dy", "gemm_wgrad", "quant_act_moe",
+               "quant_w_moe", "grouped_gemm_moe"]
+    LAUNCHES_PER_STEP = 14      # the 32 expert weights are quantized in one batched launch
 
     def __init__(self, wl, device):
         import torch
@@ -169,6 +180,7 @@ class DeviceStep:
         self.w = e((CIN, COUT), bf)
         self.dy = e((T, COUT), bf)
         self.xw = e((T, CIN), bf)
+        self.gate_up = e((T, 2 * COUT), bf)
         self.moe_x = e((wl.moe_rows, MOE_K), bf)
         self.moe_w = e((G, MOE_K, MOE_N), bf)
         self.moe_off = e((G + 1,), torch.int32)
@@ -178,6 +190,7 @@ class DeviceStep:
         self.wq_rm, self.sw_rm = e((CIN, COUT), u8), e((CIN // 128, COUT // 128), f32)
         self.dyq, self.sdy = e((T, COUT), u8), e((COUT // 128, T), f32).t()
         self.xwq, self.sxw = e((T, CIN), u8), e((CIN // 128, T), f32).t()
+        self.hq, self.sh = e((T, COUT), u8), e((COUT // 128, T), f32).t()
         self.xqT, self.sxT = e((CIN, T), u8), e((T // 128, CIN), f32).t()
         self.dyqT, self.sdyT = e((COUT, T), u8), e((T // 128, COUT), f32).t()
         self.mxq, self.smx = e((wl.moe_rows, MOE_K), u8), e((MOE_K // 128, wl.moe_rows), f32).t()
@@ -198,6 +211,7 @@ class DeviceStep:
         self.w.copy_(bf16(wl.w))
         self.dy.copy_(bf16(wl.dy))
         self.xw.copy_(bf16(wl.xw))
+        self.gate_up.copy_(bf16(wl.gate_up))
         self.moe_x.copy_(bf16(wl.moe_x))
         self.moe_w.copy_(bf16(wl.moe_w))
         self.moe_off.copy_(torch.from_numpy(wl.moe_offsets))
@@ -232,6 +246,9 @@ class DeviceStep:
         fg.fp8_gemm_blockscaled(self.dyq, self.sdy, self.wq_rm, self.sw_rm.t(), fg.FP8_SB_BLOCK128x128, self.dx,
                                 stream=stream)
         rec("gemm_dgrad", 1)
+        rec("swiglu_quant", 0)
+        fg.fp8_swiglu_quant_1x128(self.gate_up, q=self.hq, s=self.sh, stream=stream)
+        rec("swiglu_quant", 1)
         rec("quant_act_xw", 0)
         fg.fp8_quant_act_1x128(self.xw, self.xwq, self.sxw, stream=stream)
         rec("quant_act_xw", 1)
@@ -255,6 +272,41 @@ class DeviceStep:
         fg.fp8_grouped_gemm_blockscaled(self.mxq, self.smx, self.mwq, self.smw, self.moe_off, self.moe_y,
                                         stream=stream)
         rec("grouped_gemm_moe", 1)
+
+
+    def run_pow2(self, stream, ev=None):
+        """The same step with power-of-two scales: the *_pow2 quantizers and the
+        GEMMs whose scales the tensor core applies (same buffers and shapes)."""
+        fg = self.fg
+
+        def rec(name, i):
+            if ev is not None:
+                ev[name][i].record(stream)
+
+        def k(name, fn, *a, **kw):
+            rec(name, 0)
+            fn(*a, **kw)
+            rec(name, 1)
+        k("quant_act_x", fg.fp8_quant_act_1x128_pow2, self.x, self.xq, self.sx, stream=stream)
+        k("quant_w", fg.fp8_quant_w_128x128_pow2, self.w, self.wq, self.sw, stream=stream)
+        k("gemm_fprop", fg.fp8_gemm_blockscaled_mx, self.xq, self.sx, self.wq, self.sw, fg.FP8_SB_BLOCK128x128,
+          self.y, stream=stream)
+        k("quant_act_dy", fg.fp8_quant_act_1x128_pow2, self.dy, self.dyq, self.sdy, stream=stream)
+        k("quant_w_rowmajor", fg.fp8_quant_w_128x128_pow2, self.w, self.wq_rm, self.sw_rm,
+          q_layout=fg.FP8_ROWMAJOR_KN, stream=stream)
+        k("gemm_dgrad", fg.fp8_gemm_blockscaled_mx, self.dyq, self.sdy, self.wq_rm, self.sw_rm.t(),
+          fg.FP8_SB_BLOCK128x128, self.dx, stream=stream)
+        k("swiglu_quant", fg.fp8_swiglu_quant_1x128, self.gate_up, q=self.hq, s=self.sh, stream=stream)
+        k("quant_act_xw", fg.fp8_quant_act_1x128_pow2, self.xw, self.xwq, self.sxw, stream=stream)
+        k("requant_x", fg.fp8_requant_1x128_to_128x1_pow2, self.xwq, self.sxw, self.xqT, self.sxT, stream=stream)
+        k("requant_dy", fg.fp8_requant_1x128_to_128x1_pow2, self.dyq, self.sdy, self.dyqT, self.sdyT,
+          stream=stream)
+        k("gemm_wgrad", fg.fp8_gemm_blockscaled_mx, self.xqT, self.sxT, self.dyqT, self.sdyT.t(),
+          fg.FP8_SB_COL128x1, self.dw, stream=stream)
+        k("quant_act_moe", fg.fp8_quant_act_1x128_pow2, self.moe_x, self.mxq, self.smx, stream=stream)
+        k("quant_w_moe", fg.fp8_quant_w_128x128_batched_pow2, self.moe_w, self.mwq, self.smw, stream=stream)
+        k("grouped_gemm_moe", fg.fp8_grouped_gemm_blockscaled_mx, self.mxq, self.smx, self.mwq, self.smw,
+          self.moe_off, self.moe_y, stream=stream)
 
 
 # ------------------------------------------------------------- helpers ----
@@ -432,6 +484,13 @@ def cpu_oracle_sample(wl, frac, threads=1):
         t_total += dt
         est += dt * n_full / (rows * arr.shape[1])
         parts.append("act %s %d rows" % (name, rows))
+    # SwiGLU recompute + 1x128 quantization: whole rows
+    rows = max(1, int(round(frac * T)))
+    (_, dt) = timed(lambda: oracle.quant_act_1x128(
+        oracle.swiglu_bf16(wl.gate_up[:rows, :COUT], wl.gate_up[:rows, COUT:], threads=threads), threads=threads))
+    t_total += dt
+    est += dt * T / rows
+    parts.append("swiglu %d rows" % rows)
     # 128x128 weight quantization: one 128-row block strip, a fraction of its columns
     for name, arr, n_full in (("w", wl.w, CIN * COUT), ("w_rowmajor", wl.w, CIN * COUT),
                               ("moe_w", wl.moe_w[0], G * MOE_K * MOE_N)):
@@ -663,6 +722,11 @@ def main():
     if args.steady_seconds > 0:
         steady = run_steady(args, step, stream, smi_id(torch, local), ms_step, world)
 
+    # the same step with power-of-two scales and tensor-core-applied scaling
+    pow2 = None
+    if not args.no_pow2:
+        pow2 = run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, device)
+
     # end-to-end: pinned host inputs -> device -> step -> outputs back to pinned host
     e2e = None
     if not args.no_e2e:
@@ -689,13 +753,88 @@ def main():
                                 "burst": fp8_peak_burst, "nominal_at_median_clock": fp8_nominal,
                                 "source": peak_src},
             "hbm_peak_gbs": hbm,
-            "cpu_baseline": cpu, "e2e": e2e, "steady_state": steady,
+            "cpu_baseline": cpu, "e2e": e2e, "steady_state": steady, "pow2_mx": pow2,
             "gpu_launches": DeviceStep.LAUNCHES_PER_STEP * args.steps,
             "clocks": clk, "device_status": status,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def path_errors(wl, step, stream, n=2048):
+    """Error of the FP8 forward and weight-gradient outputs against the exact
+    (FP64) product of the ORIGINAL bf16 inputs, on n sampled outputs each,
+    for the promoting path (scales amax/448) and the power-of-two path:
+    relative Frobenius error and the largest error relative to rms(exact)."""
+    import torch
+    rng = np.random.default_rng(99)
+    ms, ns = rng.integers(0, T, n), rng.integers(0, COUT, n)
+    cs, os_ = rng.integers(0, CIN, n), rng.integers(0, COUT, n)
+    f64 = lambda b: synth.f32_from_bf16_bits(b).astype(np.float64)   # noqa: E731
+    exact_y = np.einsum("ik,ki->i", f64(wl.x[ms]), f64(wl.w[:, ns]))
+    exact_dw = np.einsum("ti,ti->i", f64(wl.xw[:, cs]), f64(wl.dy[:, os_]))
+    tm, tn = torch.from_numpy(ms).cuda(), torch.from_numpy(ns).cuda()
+    tc, to = torch.from_numpy(cs).cuda(), torch.from_numpy(os_).cuda()
+
+    def errs(got, ref):
+        d = got - ref
+        rms = np.sqrt(np.mean(ref ** 2))
+        return {"rel_frobenius": float(np.linalg.norm(d) / np.linalg.norm(ref)),
+                "max_abs_over_rms": float(np.max(np.abs(d)) / rms)}
+    out = {}
+    for name, run in (("amax_over_448_promoting", step.run), ("power_of_two_mx", step.run_pow2)):
+        with torch.cuda.stream(stream):
+            run(stream)
+        torch.cuda.synchronize()
+        y = step.y[tm, tn].double().cpu().numpy()
+        dw = step.dw[tc, to].double().cpu().numpy()
+        out[name] = {"forward": errs(y, exact_y), "weight_gradient": errs(dw, exact_dw)}
+    out["sample"] = "%d forward and %d weight-gradient outputs against FP64 products of the bf16 inputs" % (n, n)
+    return out
+
+
+def run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, device):
+    """Time the power-of-two step exactly as the main step is timed (warm-up,
+    args.steps steps between events, per-kernel events) and compare the two
+    paths' errors."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step.run_pow2(stream)
+    torch.cuda.synchronize()
+    evs = [{k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for k in DeviceStep.KERNELS} for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for i in range(args.steps):
+            step.run_pow2(stream, evs[i])
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = max_over_ranks(t0.elapsed_time(t1), world, device) / args.steps
+    kernels = {}
+    for k in DeviceStep.KERNELS:
+        ms = statistics.mean(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(args.steps))
+        d = {"ms": ms}
+        if k in flops:
+            tf = flops[k] / (ms * 1e-3) / 1e12
+            d.update({"tflops": tf, "frac_fp8": tf / fp8_peak})
+        else:
+            gbs = qbytes[k] / (ms * 1e-3) / 1e9
+            d.update({"gbs": gbs, "frac_hbm": gbs / hbm})
+        kernels[k] = d
+    status = step.fg.fp8_get_device_status(reset=True)
+    return {"ms_per_step": ms_step, "value": world * sum(flops.values()) / (ms_step * 1e-3) / 1e12,
+            "unit": UNIT, "kernels": kernels, "device_status": status,
+            "errors_vs_exact_bf16_product": path_errors(wl, step, stream),
+            "note": "same step, *_pow2 quantizers and the hardware block-scaled GEMMs (scales applied by "
+                    "the tensor core, no FP32 promotion); not the headline"}
 
 
 def run_steady(args, step, stream, gpu, ms_step, world):
@@ -743,12 +882,12 @@ def run_e2e(args, wl, step, stream, total_flops, world, device):
         return t.pin_memory()
     h_in = [pinned(wl.x.view(np.int16), torch.bfloat16), pinned(wl.w.view(np.int16), torch.bfloat16),
             pinned(wl.dy.view(np.int16), torch.bfloat16), pinned(wl.xw.view(np.int16), torch.bfloat16),
-            pinned(wl.moe_x.view(np.int16), torch.bfloat16),
+            pinned(wl.gate_up.view(np.int16), torch.bfloat16), pinned(wl.moe_x.view(np.int16), torch.bfloat16),
             pinned(wl.moe_w.view(np.int16), torch.bfloat16), pinned(wl.moe_offsets)]
     sets = [step, DeviceStep(wl, device)]
 
     def dev_in(st):
-        return [st.x, st.w, st.dy, st.xw, st.moe_x, st.moe_w, st.moe_off]
+        return [st.x, st.w, st.dy, st.xw, st.gate_up, st.moe_x, st.moe_w, st.moe_off]
 
     def dev_out(st):
         return [st.y, st.dx, st.dw, st.moe_y]

@@ -37,10 +37,10 @@
 //     that frees the smem stage; after the group's last K-block a commit that
 //     frees the scale slot; after the tile's last K-block a commit that hands
 //     the accumulator to the epilogue;
-//   warp 2 (both CTAs): scale loader -- reads the fp32 scales of a group of
-//     four K-blocks, converts them to UE8M0 bytes (the fp32 exponent field;
-//     any non-power-of-two scale sets FP8_ERR_DEVICE_SCALES) and writes the
-//     atoms into a shared-memory slot;
+//   warps 2 and 3 (both CTAs): scale loaders (A, B) -- read the fp32 scales
+//     of a group of four K-blocks one group ahead, convert them to UE8M0
+//     bytes (the fp32 exponent field; any non-power-of-two scale sets
+//     FP8_ERR_DEVICE_SCALES) and write the atoms into a shared-memory slot;
 //   warps 4-11 (both CTAs): epilogue -- load the whole 128 x 256 FP32
 //     accumulator of this CTA into registers (128 values per thread), release
 //     it to the MMA issuer at once, then round to bf16 and store, overlapping
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&done[i], 1);
         }
         for (int i = 0; i < SF_SLOTS; ++i) {
-            mbar_init(&sfull[i], 2);
+            mbar_init(&sfull[i], 4);    // two scale-loader warps in each CTA
             mbar_init(&sfdone[i], 1);
         }
         mbar_init(accfull, 1);
@@ -333,59 +333,81 @@ __global__ void __launch_bounds__(THREADS, 1)
             umma_commit_pair_mc(drain, 0x1);
             mbar_wait(drain, 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------ scale loader ----
-        uint32_t grp = 0;
-        bool ok = true, bad = false;
-        const uint32_t sfull_even = mapa_shared(smem_addr(&sfull[0]), 0);
-        for (int t = pair; ok && t < num_tiles; t += n_pairs) {
+    } else if (warp == 2 || warp == 3) {
+        // ----------------------------------------------- scale loaders ----
+        // warp 2: the A atom (this CTA's 128 rows); warp 3: the two B atoms
+        // (the tile's 256 columns).  Each keeps the fp32 scales of the next
+        // group of four K-blocks in registers: they are loaded right after
+        // the current group is written, so their latency overlaps the MMAs.
+        const bool is_a = warp == 2;
+        float v[2][4][KB_PER_SF];   // A: [0][i][b] row lane + 32 i; B: [h][i][b] (block scales: i = 0 only)
+        auto load = [&](int t, int gi) {
             const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
-            const int r0 = tl.row0 + static_cast<int>(rank) * BM;
-            const float* sb_base = p.sB + static_cast<int64_t>(tl.g) * p.sb_group_stride;
-            for (int gi = 0; gi < groups_per_tile; ++gi, ++grp) {
-                const uint32_t sslot = grp % SF_SLOTS, sph = (grp / SF_SLOTS) & 1u;
-                if (!__all_sync(0xffffffffu, mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns))) {
-                    if (lane == 0) signal_abort(abort_flag, peer);
-                    ok = false;
-                    break;
-                }
-                const int kb0 = gi * KB_PER_SF;
-                const int nk = min(KB_PER_SF, p.k_blocks - kb0);
-                // A atom: word i of this lane's 16-byte chunk is row lane + 32 i of this
-                // CTA's half; byte b of a word is K-block kb0 + b
-#pragma unroll 1
+            const int kb0 = gi * KB_PER_SF;
+            const int nk = min(KB_PER_SF, p.k_blocks - kb0);
+            if (is_a) {
+                const int r0 = tl.row0 + static_cast<int>(rank) * BM;
+#pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int row = r0 + lane + 32 * i;
                     const float* src = p.sA + static_cast<int64_t>(row) * p.sa_sm + static_cast<int64_t>(kb0) * p.sa_skb;
-                    uint32_t w = 0;
 #pragma unroll
-                    for (int b = 0; b < KB_PER_SF; ++b) {
-                        const float sv = (row < p.M && b < nk) ? src[static_cast<int64_t>(b) * p.sa_skb] : 0.0f;
-                        w |= ue8m0_of(sv, bad) << (8 * b);
-                    }
-                    sts_u32(sm_sfa + sslot * SFA_BYTES + 16 * lane + 4 * i, w);
+                    for (int b = 0; b < KB_PER_SF; ++b)
+                        v[0][i][b] = (row < p.M && b < nk) ? src[static_cast<int64_t>(b) * p.sa_skb] : 0.0f;
                 }
-                // B atoms: atom h covers tile columns 128 h .. 128 h + 127 (word i of the
-                // chunk: column 128 h + lane + 32 i); block scales fill an atom with one word
-#pragma unroll 1
-                for (int h = 0; h < 2; ++h) {
-#pragma unroll 1
-                    for (int i = 0; i < 4; ++i) {
+            } else {
+                const float* sb_base = p.sB + static_cast<int64_t>(tl.g) * p.sb_group_stride;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int i = 0; i < (SBK == SB_BLOCK ? 1 : 4); ++i) {
                         const int c = (SBK == SB_BLOCK) ? tl.nb * (BN / 128) + h : tl.nb * BN + 128 * h + lane + 32 * i;
                         const float* src = sb_base + static_cast<int64_t>(kb0) * p.sb_skb + static_cast<int64_t>(c) * p.sb_sn;
-                        uint32_t w = 0;
 #pragma unroll
-                        for (int b = 0; b < KB_PER_SF; ++b) {
-                            const float sv = (c < p.sb_cols && b < nk) ? src[static_cast<int64_t>(b) * p.sb_skb] : 0.0f;
-                            w |= ue8m0_of(sv, bad) << (8 * b);
-                        }
-                        sts_u32(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane + 4 * i, w);
+                        for (int b = 0; b < KB_PER_SF; ++b)
+                            v[h][i][b] = (c < p.sb_cols && b < nk) ? src[static_cast<int64_t>(b) * p.sb_skb] : 0.0f;
                     }
-                }
-                fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster_release(sfull_even + sslot * sizeof(uint64_t));
             }
+        };
+        bool bad = false;
+        auto word = [&](int h, int i) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int b = 0; b < KB_PER_SF; ++b) w |= ue8m0_of(v[h][i][b], bad) << (8 * b);
+            return w;
+        };
+        const uint32_t sfull_even = mapa_shared(smem_addr(&sfull[0]), 0);
+        int t = pair, gi = 0;
+        if (t < num_tiles) load(t, gi);
+        for (uint32_t grp = 0; t < num_tiles; ++grp) {
+            const uint32_t sslot = grp % SF_SLOTS, sph = (grp / SF_SLOTS) & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns))) {
+                if (lane == 0) signal_abort(abort_flag, peer);
+                break;
+            }
+            if (is_a) {
+                sts_v4(sm_sfa + sslot * SFA_BYTES + 16 * lane, make_uint4(word(0, 0), word(0, 1), word(0, 2), word(0, 3)));
+            } else {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    uint4 w4;
+                    if (SBK == SB_BLOCK) {
+                        const uint32_t w = word(h, 0);
+                        w4 = make_uint4(w, w, w, w);
+                    } else {
+                        w4 = make_uint4(word(h, 0), word(h, 1), word(h, 2), word(h, 3));
+                    }
+                    sts_v4(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane, w4);
+                }
+            }
+            fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_release(sfull_even + sslot * sizeof(uint64_t));
+            if (++gi == groups_per_tile) {
+                gi = 0;
+                t += n_pairs;
+            }
+            if (t < num_tiles) load(t, gi);
         }
         if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(kStatusBadScale);
       }

@@ -203,3 +203,12 @@ def moe_inputs(seed: int = 5, G: int = 32, K: int = 7168, N: int = 2048,
     w = normal_bf16(sb, (G * K, N), sigma_w).reshape(G, K, N) if with_weights else None
     return MoEInputs(x=x, w=w, counts=counts, offsets=offsets,
                      routed_rows=int(counts.sum()))
+
+
+def swiglu_inputs(seed: int, M: int, F: int, sigma: float = 1.7):
+    """Cached gate and up projections of an MLP, side by side as one bf16
+    [M, 2F] tensor (gate = columns [0, F), up = [F, 2F)), each ~ N(0, sigma^2):
+    an N(0, 1) activation times N(0, 0.02^2) weights over 7168 input channels
+    has sigma = 0.02 * sqrt(7168) = 1.7."""
+    seq = _seqs(seed, 4)[2]
+    return normal_bf16(seq, (M, 2 * F), sigma=sigma)
