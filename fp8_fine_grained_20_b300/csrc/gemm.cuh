@@ -21,7 +21,8 @@
 //   * warp 0 (both CTAs): TMA producer -- this CTA's A box (128 x 128 B) and B
 //     half (128 x 128 B), 128-byte swizzle, 5-stage ring; the transaction
 //     bytes of both CTAs are counted on the even CTA's "full" barrier;
-//   * warp 1 (even CTA): MMA issuer -- per K-block, 4 x tcgen05.mma (K = 32)
+//   * warp 1 (even CTA): MMA issuer (the whole warp runs the loop, one elected
+//     lane issues) -- per K-block, 4 x tcgen05.mma (K = 32)
 //     into one of two 256-column TMEM partial buffers, then one commit to the
 //     stage's "done" barrier in both CTAs, which both frees the smem stage for
 //     the producers and publishes the partial to the promotion warps (the
@@ -337,29 +338,35 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer ----
-        if (leader && lane == 0) {
+        // The whole warp runs the loop (warp-uniform descriptors); one elected
+        // lane, the same throughout, issues the MMAs and their commits.
+        if (leader) {
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true;
             for (int t = pair; ok && t < num_tiles; t += n_pairs) {
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     const uint32_t buf = it & 1u;
                     const uint32_t tph = (it >> 1) & 1u;
-                    if (!mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, p.wait_ns) ||
-                        !mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
-                        signal_abort(abort_flag, peer);
+                    const bool ready = mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, p.wait_ns) &&
+                                       mbar_wait(&full[stage], phase, abort_flag, p.wait_ns);
+                    if (!__all_sync(0xffffffffu, ready)) {
+                        if (lane == 0) signal_abort(abort_flag, peer);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t d = tmem + buf * BN;
-                    const uint64_t ad = sdesc_kmajor_sw128(smem_addr(sm_a + stage * A_BYTES));
-                    const uint64_t bd = sdesc_kmajor_sw128(smem_addr(sm_b + stage * B_BYTES));
+                    if (elect_one_sync()) {
+                        const uint32_t d = tmem + buf * BN;
+                        const uint64_t ad = sdesc_kmajor_sw128(smem_addr(sm_a + stage * A_BYTES));
+                        const uint64_t bd = sdesc_kmajor_sw128(smem_addr(sm_b + stage * B_BYTES));
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k) {
-                        // +32 bytes along K inside the 128-byte swizzle atom: +2 in the (>>4) address field
-                        umma_f8_pair(d, ad + 2u * k, bd + 2u * k, IDESC, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < BK / 32; ++k) {
+                            // +32 bytes along K inside the 128-byte swizzle atom: +2 in the (>>4) address field
+                            umma_f8_pair(d, ad + 2u * k, bd + 2u * k, IDESC, k > 0 ? 1u : 0u);
+                        }
+                        umma_commit_pair_mc(&done[stage], 0x3);
                     }
-                    umma_commit_pair_mc(&done[stage], 0x3);
+                    __syncwarp();
                     ++it;
                     if (++stage == STAGES) {
                         stage = 0;
@@ -367,8 +374,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            // every MMA this thread issued completes before TMEM is released
-            umma_commit_pair_mc(drain, 0x1);
+            // every MMA this warp issued completes before TMEM is released
+            if (elect_one_sync()) umma_commit_pair_mc(drain, 0x1);
+            __syncwarp();
             mbar_wait(drain, 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     } else if (warp == 2) {

@@ -277,11 +277,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1) {
         // -------------------------------------------------- MMA issuer ----
-        if (leader && lane == 0) {
+        // The whole warp runs the loop, so every descriptor and address is
+        // warp-uniform; one elected lane issues the tcgen05 instructions (the
+        // same lane throughout, as a commit tracks only its own thread's MMAs).
+        if (leader) {
             uint32_t stage = 0, phase = 0, grp = 0, tile_it = 0;
             bool ok = true;
             for (int t = pair; ok && t < num_tiles; t += n_pairs, ++tile_it) {
-                for (int kb = 0; ok && kb < p.k_blocks; ++kb) {
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
                     const uint32_t sslot = grp % SF_SLOTS, sph = (grp / SF_SLOTS) & 1u;
                     const uint32_t sfa_t = tmem + SF_TMEM_COL0 + sslot * SF_TMEM_SLOT;
                     const uint32_t sfb_t = sfa_t + 8;
@@ -289,48 +292,52 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (j == 0) {
                         // a new group: its scale atoms are in shared memory and the TMEM
                         // slot's previous group has finished its MMAs
-                        if (!mbar_wait_cluster(&sfull[sslot], sph, abort_flag, p.wait_ns) ||
-                            !mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns)) {
-                            signal_abort(abort_flag, peer);
+                        const bool ready = mbar_wait_cluster(&sfull[sslot], sph, abort_flag, p.wait_ns) &&
+                                           mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns);
+                        if (!__all_sync(0xffffffffu, ready)) {
+                            if (lane == 0) signal_abort(abort_flag, peer);
                             ok = false;
                             break;
                         }
                         tc_fence_after_sync();
-                        tc_cp_sf_pair(sfa_t, sdesc_sf_atom(smem_addr(sm_sfa + sslot * SFA_BYTES)));
-                        tc_cp_sf_pair(sfb_t, sdesc_sf_atom(smem_addr(sm_sfb + sslot * SFB_BYTES)));
-                        tc_cp_sf_pair(sfb_t + 4, sdesc_sf_atom(smem_addr(sm_sfb + sslot * SFB_BYTES + 512)));
+                        if (elect_one_sync()) {
+                            tc_cp_sf_pair(sfa_t, sdesc_sf_atom(smem_addr(sm_sfa + sslot * SFA_BYTES)));
+                            tc_cp_sf_pair(sfb_t, sdesc_sf_atom(smem_addr(sm_sfb + sslot * SFB_BYTES)));
+                            tc_cp_sf_pair(sfb_t + 4, sdesc_sf_atom(smem_addr(sm_sfb + sslot * SFB_BYTES + 512)));
+                        }
+                        __syncwarp();
                     }
-                    if (kb == 0 && !mbar_wait(accempty, (tile_it & 1u) ^ 1u, abort_flag, p.wait_ns)) {
-                        signal_abort(abort_flag, peer);
-                        ok = false;
-                        break;
-                    }
-                    if (!mbar_wait(&full[stage], phase, abort_flag, p.wait_ns)) {
-                        signal_abort(abort_flag, peer);
+                    const bool ready = (kb != 0 || mbar_wait(accempty, (tile_it & 1u) ^ 1u, abort_flag, p.wait_ns)) &&
+                                       mbar_wait(&full[stage], phase, abort_flag, p.wait_ns);
+                    if (!__all_sync(0xffffffffu, ready)) {
+                        if (lane == 0) signal_abort(abort_flag, peer);
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint64_t ad = sdesc_kmajor_sw128(smem_addr(sm_a + stage * A_BYTES));
-                    const uint64_t bd = sdesc_kmajor_sw128(smem_addr(sm_b + stage * B_BYTES));
-                    const uint32_t idesc = idesc_mx_e4m3(PM, BN, j);
+                    if (elect_one_sync()) {
+                        const uint64_t ad = sdesc_kmajor_sw128(smem_addr(sm_a + stage * A_BYTES));
+                        const uint64_t bd = sdesc_kmajor_sw128(smem_addr(sm_b + stage * B_BYTES));
+                        const uint32_t idesc = idesc_mx_e4m3(PM, BN, j);
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        umma_mx_pair(tmem, ad + 2u * k, bd + 2u * k, idesc, sfa_t, sfb_t, (kb > 0 || k > 0) ? 1u : 0u);
-                    umma_commit_pair_mc(&done[stage], 0x3);
-                    if (j == KB_PER_SF - 1 || kb == p.k_blocks - 1) {
-                        umma_commit_pair_mc(&sfdone[sslot], 0x3);
-                        ++grp;
+                        for (int k = 0; k < BK / 32; ++k)
+                            umma_mx_pair(tmem, ad + 2u * k, bd + 2u * k, idesc, sfa_t, sfb_t,
+                                         (kb > 0 || k > 0) ? 1u : 0u);
+                        umma_commit_pair_mc(&done[stage], 0x3);
+                        if (j == KB_PER_SF - 1 || kb == p.k_blocks - 1) umma_commit_pair_mc(&sfdone[sslot], 0x3);
+                        if (kb == p.k_blocks - 1) umma_commit_pair_mc(accfull, 0x3);
                     }
-                    if (kb == p.k_blocks - 1) umma_commit_pair_mc(accfull, 0x3);
+                    __syncwarp();
+                    if (j == KB_PER_SF - 1 || kb == p.k_blocks - 1) ++grp;
                     if (++stage == MX_STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
-            // every copy and MMA this thread issued completes before TMEM is released
-            umma_commit_pair_mc(drain, 0x1);
+            // every copy and MMA this warp issued completes before TMEM is released
+            if (elect_one_sync()) umma_commit_pair_mc(drain, 0x1);
+            __syncwarp();
             mbar_wait(drain, 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     } else if (warp == 2 || warp == 3) {

@@ -136,6 +136,18 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// One lane of a converged warp (the same lane on every call with the full
+// mask): the issuer of a warp-uniform tcgen05 loop.
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // Spin for about `ns` nanoseconds (bounded by the global timer).
 __device__ __forceinline__ void spin_ns(uint64_t ns) {
     const uint64_t t0 = global_timer_ns();

@@ -10,11 +10,13 @@
 // value an unfused SwiGLU would store), so the output never goes through HBM
 // in bf16; the bf16 y can optionally be written as well.
 //
-// Arithmetic per element, in fp32 with no overflow for any finite input:
-// e = 2^(-|g| log2 e) (MUFU ex2), r = 1 / (1 + e) (MUFU rcp), sigma(g) = r for
-// g >= 0 and e r for g < 0, y = (g sigma) u, rounded to bf16 (nearest even).
-// While |g| <= 87 (sigma stays a normal fp32 number) this is within one bf16
-// ulp of the correctly rounded SwiGLU value.  The bf16 values are then
+// Arithmetic per pair of elements, in fp32 (packed FP32x2 where it exists):
+// e = 2^(-g log2 e) (MUFU ex2, flushing subnormal results), sigma = 1 / (1 + e)
+// (MUFU rcp), y = (g sigma) u, rounded to bf16 (nearest even).  For g below
+// about -88.7, e overflows to infinity and sigma is 0; for g above about 87, e
+// flushes to 0 and sigma is 1.  While |g| <= 87 (sigma stays a normal fp32
+// number) the result is within one bf16 ulp of the correctly rounded SwiGLU
+// value.  The bf16 values are then
 // quantized exactly as k_quant_act_1x128 quantizes its input (amax, the IEEE
 // scale, exact quotients), so the codes equal the 1x128 quantization of the
 // bf16 y bit for bit.
@@ -42,43 +44,35 @@ struct SwigluArgs {
     int M, FB;
 };
 
-__device__ __forceinline__ float ex2_approx(float x) {
+__device__ __forceinline__ float ex2_ftz(float x) {
     float r;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
 
-__device__ __forceinline__ float rcp_approx(float x) {
+__device__ __forceinline__ float rcp_ftz(float x) {
     float r;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
 
-// silu(g) * u for one element (see the file comment).
-__device__ __forceinline__ float swiglu1(float g, float u) {
-    const float e = ex2_approx(-fabsf(g) * 1.4426950408889634f);
-    const float r = rcp_approx(1.0f + e);
-    const float sig = (g >= 0.0f) ? r : e * r;
-    return (g * sig) * u;
+// silu(g) * u of a bf16x2 gate word and a bf16x2 up word -> bf16x2.
+__device__ __forceinline__ uint32_t swiglu2(uint32_t gw, uint32_t uw) {
+    constexpr float kNegLog2e = -1.4426950408889634f;
+    const float2 g = bf16x2_to_f32x2(gw);
+    const float2 u = bf16x2_to_f32x2(uw);
+    const float2 a = __fmul2_rn(g, make_float2(kNegLog2e, kNegLog2e));
+    const float2 d = __fadd2_rn(make_float2(ex2_ftz(a.x), ex2_ftz(a.y)), make_float2(1.0f, 1.0f));
+    const float2 y = __fmul2_rn(__fmul2_rn(g, make_float2(rcp_ftz(d.x), rcp_ftz(d.y))), u);
+    uint32_t w;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(y.y), "f"(y.x));
+    return w;
 }
 
 // Eight bf16 gate and eight bf16 up values (one 16-byte chunk each) -> the
 // eight bf16 SwiGLU outputs, packed as four bf16x2 words.
 __device__ __forceinline__ uint4 swiglu8(const uint4& gv, const uint4& uv) {
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float2 g2 = bf16x2_to_f32x2(gw[k]);
-        const float2 u2 = bf16x2_to_f32x2(uw[k]);
-        const float lo = swiglu1(g2.x, u2.x);
-        const float hi = swiglu1(g2.y, u2.y);
-        uint32_t w;
-        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(w) : "f"(hi), "f"(lo));
-        o[k] = w;
-    }
-    return make_uint4(o[0], o[1], o[2], o[3]);
+    return make_uint4(swiglu2(gv.x, uv.x), swiglu2(gv.y, uv.y), swiglu2(gv.z, uv.z), swiglu2(gv.w, uv.w));
 }
 
 template <int UNROLL>

@@ -279,3 +279,33 @@ def swiglu_bf16(gate, up, threads=None):
     if undecided:
         raise ValueError("oracle swiglu_bf16: %d roundings could not be decided" % undecided)
     return y
+
+
+def dequant_dense(q, s, axis_groups):
+    """FP64 values of codes q [R, C] with scales s: axis_groups=1 -> s [R, C/128]
+    (groups along columns), 0 -> s [R/128, C/128] blocks.  Exact in FP64."""
+    lib = _load()
+    table = np.array([lib.orc_e4m3_decode(c) for c in range(256)], np.float64)
+    v = table[np.asarray(q, np.uint8)]
+    s = np.asarray(s, np.float64)
+    if axis_groups == 1:
+        v *= np.repeat(s, 128, axis=1)
+    else:
+        v *= np.repeat(np.repeat(s, 128, axis=0), 128, axis=1)
+    return v
+
+
+def gemm_blockscaled_dense(A, sA, Bt, sB, sb_kind=SB_BLOCK128x128):
+    """The block-scaled GEMM as the FP64 matrix product of the dequantized
+    operands (reading R6: the promotion interval equals the quantization group,
+    so the result is exactly that product), with numpy's float64 matmul as the
+    summation step.  Same arguments as gemm_blockscaled; the summation order
+    differs from it only by FP64 rounding."""
+    A, Bt = np.asarray(A, np.uint8), np.asarray(Bt, np.uint8)
+    sA, sB = np.asarray(sA, np.float32), np.asarray(sB, np.float32)
+    a = dequant_dense(A, sA, 1)
+    if sb_kind == SB_COL128x1:
+        b = dequant_dense(Bt, np.ascontiguousarray(sB.T), 1)          # sB [K/128, N] -> per row of Bt
+    else:
+        b = dequant_dense(Bt, np.ascontiguousarray(sB.T), 0)          # sB [K/128, N/128] -> blocks of Bt
+    return a @ b.T

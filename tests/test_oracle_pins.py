@@ -390,3 +390,23 @@ def test_grouped_gemm_matches_per_expert_numpy(orc):
     ns = np.array([0, 5, 255, 128, 1])
     smp = orc.grouped_gemm_blockscaled_sample(qa, sa, qb, sb, offsets, ms, ns)
     assert np.array_equal(smp[:4], C[ms[:4], ns[:4]]) and np.isnan(smp[4])
+
+
+def test_dense_gemm_form_matches_elementwise_oracle(orc):
+    """The dense FP64 form used for full-size acceptance equals the plain
+    element-wise oracle up to FP64 summation order, for both scale kinds."""
+    a, b, _ = synth.tiny_end_to_end(seed=1)
+    qa, sa = orc.quant_act_1x128(a)
+    qb, sb = orc.quant_w_128x128(b)
+    qbt = np.ascontiguousarray(qb.T)
+    ref = orc.gemm_blockscaled(qa, sa, qbt, sb, orc.SB_BLOCK128x128)
+    got = orc.gemm_blockscaled_dense(qa, sa, qbt, sb, orc.SB_BLOCK128x128)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))
+    x = synth.wgrad_tensor(3, 0, 256, 128)
+    dy = synth.wgrad_tensor(3, 1, 256, 256)
+    qx, sx = orc.requant_1x128_to_128x1(*orc.quant_act_1x128(x))
+    qd, sd = orc.requant_1x128_to_128x1(*orc.quant_act_1x128(dy))
+    sb_col = np.ascontiguousarray(sd.T)
+    ref = orc.gemm_blockscaled(qx, sx, qd, sb_col, orc.SB_COL128x1)
+    got = orc.gemm_blockscaled_dense(qx, sx, qd, sb_col, orc.SB_COL128x1)
+    assert np.max(np.abs(got - ref)) <= 1e-12 * np.max(np.abs(ref))
