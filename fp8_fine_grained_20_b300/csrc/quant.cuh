@@ -118,6 +118,21 @@ __device__ __forceinline__ uint32_t quant_div(float x, float s, int mode) {
     return c | ((__float_as_uint(x) >> 24) & 0x80u);
 }
 
+// RN(x / s) for a pair of bf16 dividends (8 significant bits): one correction
+// step suffices, q0 = x r;  q = q0 + (x - q0 s) r.  With bf16 x and s = RN(amax
+// / 448) for bf16 amax, the quotient depends only on the two significands and
+// the exponent gap (every step scales exactly with a power of two while the
+// scale is at least 2^-92), and the parity tests compare this quotient's
+// codes with IEEE division over every bf16 significand pair and every gap at
+// which a code can be nonzero, so the single step is exact for every input
+// these quantizers accept.  fp32 dividends (the requantizer's) take the two
+// steps above.
+__device__ __forceinline__ float2 div2_markstein_bf16(float2 x, float2 r2, float2 ns2) {
+    const float2 q0 = __fmul2_rn(x, r2);
+    const float2 e0 = __ffma2_rn(q0, ns2, x);
+    return __ffma2_rn(e0, r2, q0);
+}
+
 // RN(x / s) of a pair: Markstein's correction, or one multiply by r = 1/s
 // when s is a power of two (then x r is the exact quotient, rounded once).
 template <bool POW2>
@@ -126,16 +141,22 @@ __device__ __forceinline__ float2 div2_t(float2 x, float2 r2, float2 ns2) {
     return div2_markstein(x, r2, ns2);
 }
 
+template <bool POW2>
+__device__ __forceinline__ float2 div2_bf16_t(float2 x, float2 r2, float2 ns2) {
+    if (POW2) return __fmul2_rn(x, r2);
+    return div2_markstein_bf16(x, r2, ns2);
+}
+
 // Eight codes of eight bf16 values (one 16-byte chunk) of one group.
 template <bool POW2 = false>
 __device__ __forceinline__ uint2 quant8_bf16(const uint4& v, const GroupScale& g) {
     if (g.mode == 1) {
         const float2 r2 = make_float2(g.r, g.r);
         const float2 ns2 = make_float2(-g.s, -g.s);
-        const uint32_t c0 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.x), r2, ns2));
-        const uint32_t c1 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.y), r2, ns2));
-        const uint32_t c2 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.z), r2, ns2));
-        const uint32_t c3 = e4m3_pair(div2_t<POW2>(bf16x2_to_f32x2(v.w), r2, ns2));
+        const uint32_t c0 = e4m3_pair(div2_bf16_t<POW2>(bf16x2_to_f32x2(v.x), r2, ns2));
+        const uint32_t c1 = e4m3_pair(div2_bf16_t<POW2>(bf16x2_to_f32x2(v.y), r2, ns2));
+        const uint32_t c2 = e4m3_pair(div2_bf16_t<POW2>(bf16x2_to_f32x2(v.z), r2, ns2));
+        const uint32_t c3 = e4m3_pair(div2_bf16_t<POW2>(bf16x2_to_f32x2(v.w), r2, ns2));
         // sign bits (bit 15 of each bf16) into bit 7 of each code byte
         const uint32_t sx = __byte_perm(v.x, v.y, 0x7531) & 0x80808080u;
         const uint32_t sy = __byte_perm(v.z, v.w, 0x7531) & 0x80808080u;
