@@ -7,6 +7,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/fp8fg.h"
@@ -88,6 +89,21 @@ bool make_kmajor_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t co
     const cuuint32_t estr[2] = {1u, 1u};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// bf16 [rows][cols] output (row stride ld elements) written by 32-row x
+// 64-column TMA stores from 128-byte-swizzled staging tiles.
+bool make_c_store_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int64_t ld) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * 2)};
+    const cuuint32_t box[2] = {64u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -176,10 +192,13 @@ fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const ui
     const fp8_status_t rc =
         pair_config(kernel, GROUPED ? gemm::SMEM_GROUPED : gemm::SMEM_PLAIN, st, args, GROUPED, stream, cfg, attr);
     if (rc != FP8_OK) return rc;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
     if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
     if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BNH)) return FP8_ERR_CUDA;
-    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args, qargs) != cudaSuccess) {
+    memset(&tmC, 0, sizeof(tmC));
+    if (SBK == gemm::SB_BLOCK && !QOUT && !make_c_store_map(&tmC, args.C, args.M, args.N, args.ldc))
+        return FP8_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args, qargs) != cudaSuccess) {
         cudaGetLastError();
         return FP8_ERR_CUDA;
     }

@@ -68,9 +68,14 @@ constexpr uint32_t IDESC = idesc_e4m3_f32(PM, BN);
 constexpr int SB_BLOCK = 0;  // sB[kb][n/128]
 constexpr int SB_COL = 1;    // sB[kb][n]
 
+// bf16 epilogue staging: one 32-row x 64-column tile (4 KB, 128-byte TMA
+// swizzle) per promotion warp
+constexpr uint32_t C_STAGE_BYTES = 32 * 64 * 2;
+
 constexpr size_t OFF_A = 0;
 constexpr size_t OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr size_t OFF_SA = OFF_B + STAGES * B_BYTES;
+constexpr size_t OFF_C = OFF_B + STAGES * B_BYTES;
+constexpr size_t OFF_SA = OFF_C + PROMO_WARPS * C_STAGE_BYTES;
 constexpr size_t OFF_SB = OFF_SA + SSLOTS * BM * sizeof(float);
 constexpr size_t OFF_BAR = OFF_SB + SSLOTS * BN * sizeof(float);
 constexpr int N_BARS = 2 * STAGES + 2 + 2 * SSLOTS + 1;
@@ -228,11 +233,12 @@ __device__ __forceinline__ void signal_abort(volatile int* abort_flag, uint32_t 
 template <int SBK, bool GROUPED, bool QOUT = false>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_blockscaled(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const Args p, const QArgs qo) {
+                       const __grid_constant__ CUtensorMap tmC, const Args p, const QArgs qo) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sm_a = base + OFF_A;
     uint8_t* sm_b = base + OFF_B;
+    uint8_t* sm_c = base + OFF_C;
     float* sm_sa = reinterpret_cast<float*>(base + OFF_SA);
     float* sm_sb = reinterpret_cast<float*>(base + OFF_SB);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + OFF_BAR);
@@ -271,6 +277,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (SBK == SB_BLOCK && !QOUT) tma_prefetch_desc(&tmC);
     }
     if (GROUPED) {
         for (int i = threadIdx.x; i <= p.G; i += THREADS) goff[i] = p.offsets[i];
@@ -442,6 +449,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t it = 0;   // K-blocks promoted so far; every ring position derives from it
         bool ok = true;
         for (int t = pair; ok && t < num_tiles; t += n_pairs) {
+            // the tile's place, found before the K-loop (the grouped search then runs
+            // while few registers are live)
+            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
@@ -515,7 +525,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(&sempty[slot]);
             }
             if (!ok) break;
-            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
             const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
             const int n0 = tl.nb * BN + half * 128;
             if constexpr (SBK == SB_COL) {
@@ -605,18 +614,34 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 qo.sC[static_cast<int64_t>(grow) * qo.sc_m + static_cast<int64_t>(n0 / 128) * qo.sc_nb] = gs.s;
             } else {
-                uint16_t* crow = p.C + static_cast<int64_t>(grow) * p.ldc + n0;
+                // the warp's 32 rows x 128 columns in two 32 x 64 TMA stores: each lane
+                // writes its row into the swizzled staging tile (16-byte chunk j of row r
+                // at chunk j ^ (r % 8): conflict-free), then lane 0 issues the store
+                uint8_t* stg = sm_c + (warp - 4) * C_STAGE_BYTES;
+                const int wrow0 = tl.row0 + static_cast<int>(rank) * BM + quarter * 32;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    uint4 w;
-                    w.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
-                    w.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
-                    w.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
-                    w.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
-                    stg_v4(crow + 8 * j, w);
+                for (int h = 0; h < 2; ++h) {
+                    if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int o = 64 * h + 8 * j;
+                        sts_v4(stg + lane * 128 + ((j ^ (lane & 7)) << 4),
+                               make_uint4(pack_bf16x2(acc[o + 0], acc[o + 1]), pack_bf16x2(acc[o + 2], acc[o + 3]),
+                                          pack_bf16x2(acc[o + 4], acc[o + 5]), pack_bf16x2(acc[o + 6], acc[o + 7])));
+                    }
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, stg, n0 + 64 * h, wrow0);
+                        bulk_commit_group();
+                    }
                 }
             }
         }
+        // every store of this warp has completed before its staging tile is released
+        if (SBK == SB_BLOCK && !QOUT && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     // Teardown.  After the first cluster barrier no thread of either CTA waits

@@ -426,6 +426,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int row = quarter * 32 + lane;
         uint32_t tile_it = 0;
         for (int t = pair; t < num_tiles; t += n_pairs, ++tile_it) {
+            // the tile's place, found while no accumulator values are live
+            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
+            const int n0 = tl.nb * BN + half * 128;
+            const bool store = grow < tl.row_end && n0 < p.N;
             if (!__all_sync(0xffffffffu, mbar_wait(accfull, tile_it & 1u, abort_flag, p.wait_ns))) {
                 if (lane == 0) signal_abort(abort_flag, peer);
                 break;
@@ -442,10 +447,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(accempty), 0));   // the even CTA's
-            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
-            const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
-            const int n0 = tl.nb * BN + half * 128;
-            if (!(grow < tl.row_end && n0 < p.N)) continue;
+            if (!store) continue;
             uint16_t* crow = p.C + static_cast<int64_t>(grow) * p.ldc + n0;
             auto store32 = [&](const uint32_t (&r)[32], int c0) {
 #pragma unroll

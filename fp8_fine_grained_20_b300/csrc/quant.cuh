@@ -141,6 +141,21 @@ __device__ __forceinline__ float2 div2_t(float2 x, float2 r2, float2 ns2) {
     return div2_markstein(x, r2, ns2);
 }
 
+// RN(x / s) of a pair given NEGATED dividends nx = -x, nr2 = (-RN(1/s), ..)
+// and s2 = (s, s): the same two correction steps as div2_markstein, written
+// as e = q s + nx, q <- e (-r) + q.  Value for value this is div2_markstein;
+// in addition the sign of a zero dividend survives (x = -0 gives -0, not +0),
+// so no sign bits need to be restored after the E4M3 conversion.  With a
+// power-of-two s the quotient is the single exact product nx (-r).
+template <bool POW2>
+__device__ __forceinline__ float2 div2_neg_t(float2 nx, float2 nr2, float2 s2) {
+    float2 q = __fmul2_rn(nx, nr2);
+    if (POW2) return q;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) q = __ffma2_rn(__ffma2_rn(q, s2, nx), nr2, q);
+    return q;
+}
+
 template <bool POW2>
 __device__ __forceinline__ float2 div2_bf16_t(float2 x, float2 r2, float2 ns2) {
     if (POW2) return __fmul2_rn(x, r2);
@@ -455,9 +470,11 @@ __global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_
 // tile ([16 channels][128 tokens]) with one 2-byte store; the tile's 16-byte
 // chunks are XOR-swizzled by channel pair, so the eight channel rows written
 // by one store land in distinct banks.  The warp then copies its 16 output
-// rows out with 16-byte stores, eight lanes per 128-byte row.  The sign bit
-// of every code is that of its dequantized value (the input code's sign, as
-// the row scales are not negative).
+// rows out with 16-byte stores, eight lanes per 128-byte row.  Pass 1 keeps
+// the dequantized values negated (the code's sign bit flipped before the
+// multiply, which is exact), because the division written on negated
+// dividends keeps the sign of a zero value, so every code comes out of the
+// E4M3 conversion with its sign already right.
 constexpr int RQ_STAGES = 4;
 constexpr int RQ_WARPS = 8;                       // 16 channels each
 constexpr int RQ_THREADS = 32 * RQ_WARPS;
@@ -484,6 +501,11 @@ __device__ __forceinline__ uint32_t lds_u16(const void* p) {
 
 __device__ __forceinline__ void sts_u16(void* p, uint32_t v) {
     asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_addr(p)), "h"(static_cast<uint16_t>(v)) : "memory");
+}
+
+// 2-byte shared store at a shared::cta address.
+__device__ __forceinline__ void sts_u16_at(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(static_cast<uint16_t>(v)) : "memory");
 }
 
 template <bool POW2 = false>
@@ -565,7 +587,8 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
         const uint8_t* tile = tiles + stage * RQ_TILE_BYTES;
         const float* srow = sc + stage * 128;
 
-        // pass 1: dequantize rows 8a+2g+b, channels 2c, 2c+1; per-channel amax
+        // pass 1: dequantize rows 8a+2g+b, channels 2c, 2c+1 (kept negated,
+        // -xhat, for the sign-preserving division below); per-channel amax
         float xv[16][4];     // [a][2b + j]
         float am0 = 0.0f, am1 = 0.0f;
 #pragma unroll
@@ -575,8 +598,9 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
             const uint32_t lo = lds_u16(tile + r0 * 128 + ((w ^ (2 * g)) << 4) + 2 * c);
             const uint32_t hi = lds_u16(tile + (r0 + 1) * 128 + ((w ^ (2 * g + 1)) << 4) + 2 * c);
             const float2 s2 = *reinterpret_cast<const float2*>(srow + r0);
-            const uint32_t h0 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(lo));
-            const uint32_t h1 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(hi));
+            // the negated codes (sign bits flipped) times the row scale: -xhat, exactly
+            const uint32_t h0 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(lo)) ^ 0x80008000u;
+            const uint32_t h1 = cvt_e4m3x2_to_f16x2(static_cast<uint16_t>(hi)) ^ 0x80008000u;
             const float2 p0 = __fmul2_rn(make_float2(f16_bits_to_f32(h0 & 0xFFFFu), f16_bits_to_f32(h0 >> 16)),
                                          make_float2(s2.x, s2.x));
             const float2 p1 = __fmul2_rn(make_float2(f16_bits_to_f32(h1 & 0xFFFFu), f16_bits_to_f32(h1 >> 16)),
@@ -607,27 +631,29 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
             chm[j] = __shfl_sync(0xffffffffu, gs.mode, c + 8 * j);
         }
 
-        // pass 2: codes of rows (8a+2g, 8a+2g+1) are bytes 8a+2g, +1 of output row 2c+j
+        // pass 2: codes of rows (8a+2g, 8a+2g+1) are bytes 8a+2g, +1 of output row 2c+j.
+        // Output row 2c+j starts 128-aligned in the warp's tile; its 16-byte chunk a/2
+        // sits at chunk (a/2) ^ c, so with b = row base | c << 4 | 2g (disjoint bits) the
+        // store address is b ^ ((a/2) << 4), one XOR with an immediate, plus 8 (a & 1).
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            uint8_t* orow = wst + (2 * c + j) * 128;
+            const uint32_t ob = smem_addr(wst + (2 * c + j) * 128) | (static_cast<uint32_t>(c) << 4) |
+                                static_cast<uint32_t>(2 * g);
             if (chm[j] == 1) {
-                const float2 r2 = make_float2(chr[j], chr[j]);
-                const float2 ns2 = make_float2(-chs[j], -chs[j]);
+                const float2 nr2 = make_float2(-chr[j], -chr[j]);
+                const float2 s2 = make_float2(chs[j], chs[j]);
 #pragma unroll
                 for (int aa = 0; aa < 16; ++aa) {
-                    const uint32_t code = e4m3_pair(div2_t<POW2>(make_float2(xv[aa][j], xv[aa][2 + j]), r2, ns2));
-                    // sign bits of the two dequantized values: bit 7 of their top bytes
-                    const uint32_t top =
-                        __byte_perm(__float_as_uint(xv[aa][j]), __float_as_uint(xv[aa][2 + j]), 0x0073);
-                    sts_u16(orow + (((aa >> 1) ^ c) << 4) + 8 * (aa & 1) + 2 * g, code | (top & 0x8080u));
+                    const uint32_t code =
+                        e4m3_pair(div2_neg_t<POW2>(make_float2(xv[aa][j], xv[aa][2 + j]), nr2, s2));
+                    sts_u16_at((ob ^ static_cast<uint32_t>((aa >> 1) << 4)) + 8 * (aa & 1), code);
                 }
             } else {
 #pragma unroll
                 for (int aa = 0; aa < 16; ++aa) {
-                    const uint32_t code = quant_div(xv[aa][j], chs[j], chm[j]) |
-                                          (quant_div(xv[aa][2 + j], chs[j], chm[j]) << 8);
-                    sts_u16(orow + (((aa >> 1) ^ c) << 4) + 8 * (aa & 1) + 2 * g, code);
+                    const uint32_t code = quant_div(-xv[aa][j], chs[j], chm[j]) |
+                                          (quant_div(-xv[aa][2 + j], chs[j], chm[j]) << 8);
+                    sts_u16_at((ob ^ static_cast<uint32_t>((aa >> 1) << 4)) + 8 * (aa & 1), code);
                 }
             }
         }
