@@ -196,7 +196,7 @@ fp8_status_t launch_gemm(const uint8_t* A, int64_t lda, int64_t a_rows, const ui
     if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
     if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BNH)) return FP8_ERR_CUDA;
     memset(&tmC, 0, sizeof(tmC));
-    if (SBK == gemm::SB_BLOCK && !QOUT && !make_c_store_map(&tmC, args.C, args.M, args.N, args.ldc))
+    if (!QOUT && !make_c_store_map(&tmC, args.C, args.M, args.N, args.ldc))
         return FP8_ERR_CUDA;
     if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args, qargs) != cudaSuccess) {
         cudaGetLastError();

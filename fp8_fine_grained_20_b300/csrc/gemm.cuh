@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
-        if (SBK == SB_BLOCK && !QOUT) tma_prefetch_desc(&tmC);
+        if (!QOUT) tma_prefetch_desc(&tmC);
     }
     if (GROUPED) {
         for (int i = threadIdx.x; i <= p.G; i += THREADS) goff[i] = p.offsets[i];
@@ -531,11 +531,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // rows and groups are whole 128-row blocks: the test is uniform per CTA
                 const int g0 = tl.row0 + static_cast<int>(rank) * BM + quarter * 32 + r4;
                 if (!(tl.row0 + static_cast<int>(rank) * BM < tl.row_end && n0 < p.N)) continue;
+                if constexpr (QOUT) {
 #pragma unroll
                 for (int rs = 0; rs < 4; ++rs) {          // rows g0 + 16 (rs >> 1) + 8 (rs & 1)
                     const int grw = g0 + 16 * (rs >> 1) + 8 * (rs & 1);
                     const int e = rs & 1, lh = rs >> 1;
-                    if constexpr (QOUT) {
                         // the row's 128 columns sit in the four lanes of this quad
                         uint32_t w[16];
 #pragma unroll
@@ -568,27 +568,45 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (q4 == 0)
                             qo.sC[static_cast<int64_t>(grw) * qo.sc_m + static_cast<int64_t>(n0 / 128) * qo.sc_nb] =
                                 gs.s;
-                    } else {
-                        // 4x4 transposes of bf16 across the quad, two shuffles each: lane q
-                        // then holds columns 4(4g + q) .. +3 and writes them with one 8-byte store
-                        uint16_t* crow = p.C + static_cast<int64_t>(grw) * p.ldc + n0 + 4 * q4;
-                        const uint32_t sel_w0 = (q4 == 0) ? 0x5410u : (q4 == 1) ? 0x3254u : (q4 == 2) ? 0x7610u : 0x3276u;
-                        const uint32_t sel_w1 = (q4 == 0) ? 0x7610u : (q4 == 1) ? 0x3276u : (q4 == 2) ? 0x5410u : 0x3254u;
+                }
+                } else {
+                    // 4x4 transposes of bf16 across the quad, two shuffles each: lane q then
+                    // holds columns 4(4g + q) .. +3 of a row; the 8 bytes go into the warp's
+                    // swizzled 32 x 64 staging tile (row r: 16-byte chunk j at j ^ (r % 8)),
+                    // one TMA store per 64 columns
+                    uint8_t* stg = sm_c + (warp - 4) * C_STAGE_BYTES;
+                    const int wrow0 = tl.row0 + static_cast<int>(rank) * BM + quarter * 32;
+                    const uint32_t sel_w0 = (q4 == 0) ? 0x5410u : (q4 == 1) ? 0x3254u : (q4 == 2) ? 0x7610u : 0x3276u;
+                    const uint32_t sel_w1 = (q4 == 0) ? 0x7610u : (q4 == 1) ? 0x3276u : (q4 == 2) ? 0x5410u : 0x3254u;
 #pragma unroll
-                        for (int c = 0; c < 2; ++c)
+                    for (int c = 0; c < 2; ++c) {
+                        if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
+                        __syncwarp();
+#pragma unroll
+                        for (int rs = 0; rs < 4; ++rs) {      // local rows 16 (rs >> 1) + 8 (rs & 1) + r4
+                            const int e = rs & 1, lh = rs >> 1;
+                            const int rl = 16 * lh + 8 * e + r4;
 #pragma unroll
                             for (int g = 0; g < 4; ++g) {
-                                const float* v = acc + 32 * (2 * c + lh) + 8 * g + e;   // v[2k]: column 4(4g+k) + q
-                                const uint32_t p0 = pack_bf16x2(v[0], v[2]);
-                                const uint32_t p1 = pack_bf16x2(v[4], v[6]);
+                                const int o = 32 * (2 * c + lh) + 8 * g + e;   // acc[o + 2k]: column 4(4g+k) + q
+                                const uint32_t p0 = pack_bf16x2(acc[o + 0], acc[o + 2]);
+                                const uint32_t p1 = pack_bf16x2(acc[o + 4], acc[o + 6]);
                                 const uint32_t x = (q4 & 2) ? p1 : p0;
                                 const uint32_t y = __shfl_xor_sync(0xffffffffu, (q4 & 2) ? p0 : p1, 2);
                                 const uint32_t rr =
                                     __shfl_xor_sync(0xffffffffu, __byte_perm(x, y, (q4 & 1) ? 0x5410u : 0x7632u), 1);
                                 const uint32_t a = (q4 & 2) ? y : x;
                                 const uint32_t b = (q4 & 2) ? x : y;
-                                stg_v2(crow + 64 * c + 16 * g, make_uint2(__byte_perm(a, rr, sel_w0), __byte_perm(b, rr, sel_w1)));
+                                sts_v2(stg + rl * 128 + (((2 * g + (q4 >> 1)) ^ r4) << 4) + (q4 & 1) * 8,
+                                       make_uint2(__byte_perm(a, rr, sel_w0), __byte_perm(b, rr, sel_w1)));
                             }
+                        }
+                        fence_proxy_async_shared();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, stg, n0 + 64 * c, wrow0);
+                            bulk_commit_group();
+                        }
                     }
                 }
                 continue;
@@ -640,7 +658,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
         // every store of this warp has completed before its staging tile is released
-        if (SBK == SB_BLOCK && !QOUT && lane == 0) bulk_wait_all();
+        if (!QOUT && lane == 0) bulk_wait_all();
         __syncwarp();
     }
 
