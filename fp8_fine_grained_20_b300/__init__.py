@@ -54,7 +54,10 @@ __all__ = [
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(HERE, "libfp8fg.so")
+# FP8FG_BOUNDS=1 selects the debug build in which every device write is
+# bounds-checked (an out-of-tile write is skipped and reported as
+# FP8_ERR_DEVICE_BOUNDS in the device status word)
+library_path = os.path.join(HERE, "libfp8fg_bounds.so" if os.environ.get("FP8FG_BOUNDS") == "1" else "libfp8fg.so")
 
 FP8_OK = 0
 FP8_KMAJOR_NK = 0
@@ -65,7 +68,7 @@ FP8_SB_COL128x1 = 1
 STATUS_NAMES = {
     0: "FP8_OK", 1: "FP8_ERR_NULL", 2: "FP8_ERR_ALIGN", 3: "FP8_ERR_SHAPE", 4: "FP8_ERR_CUDA",
     5: "FP8_ERR_DEVICE_TIMEOUT", 6: "FP8_ERR_ARG", 7: "FP8_ERR_DEVICE", 8: "FP8_ERR_DEVICE_GROUPS",
-    9: "FP8_ERR_DEVICE_SCALES",
+    9: "FP8_ERR_DEVICE_SCALES", 10: "FP8_ERR_DEVICE_BOUNDS",
 }
 
 # (name, argtypes) of every exported function; restype fp8_status_t (int) unless noted

@@ -254,6 +254,7 @@ const char* fp8_status_string(fp8_status_t s) {
         case FP8_ERR_DEVICE: return "FP8_ERR_DEVICE: unsupported device or resource limit";
         case FP8_ERR_DEVICE_GROUPS: return "FP8_ERR_DEVICE_GROUPS: invalid group offsets seen on the device";
         case FP8_ERR_DEVICE_SCALES: return "FP8_ERR_DEVICE_SCALES: a scale given to an _mx GEMM is not a power of two";
+        case FP8_ERR_DEVICE_BOUNDS: return "FP8_ERR_DEVICE_BOUNDS: a device write fell outside its tile (bounds-checked build)";
     }
     return "unknown fp8fg status";
 }

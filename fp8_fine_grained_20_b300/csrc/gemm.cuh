@@ -562,10 +562,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     gs);
 #pragma unroll
                                 for (int b = 0; b < 8; ++b)
-                                    qrow[64 * c + 4 * (8 * k + b)] =
-                                        static_cast<uint8_t>(((b < 4 ? cd.x : cd.y) >> (8 * (b & 3))) & 0xFFu);
+                                    if (FP8_IN_BOUNDS(grw < p.M && n0 + q4 + 64 * c + 4 * (8 * k + b) < p.N))
+                                        qrow[64 * c + 4 * (8 * k + b)] =
+                                            static_cast<uint8_t>(((b < 4 ? cd.x : cd.y) >> (8 * (b & 3))) & 0xFFu);
                             }
-                        if (q4 == 0)
+                        if (q4 == 0 && FP8_IN_BOUNDS(grw < p.M && n0 < p.N))
                             qo.sC[static_cast<int64_t>(grw) * qo.sc_m + static_cast<int64_t>(n0 / 128) * qo.sc_nb] =
                                 gs.s;
                 }
@@ -597,13 +598,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     __shfl_xor_sync(0xffffffffu, __byte_perm(x, y, (q4 & 1) ? 0x5410u : 0x7632u), 1);
                                 const uint32_t a = (q4 & 2) ? y : x;
                                 const uint32_t b = (q4 & 2) ? x : y;
-                                sts_v2(stg + rl * 128 + (((2 * g + (q4 >> 1)) ^ r4) << 4) + (q4 & 1) * 8,
-                                       make_uint2(__byte_perm(a, rr, sel_w0), __byte_perm(b, rr, sel_w1)));
+                                const uint32_t off = rl * 128 + (((2 * g + (q4 >> 1)) ^ r4) << 4) + (q4 & 1) * 8;
+                                if (FP8_IN_BOUNDS(off + 8 <= C_STAGE_BYTES))
+                                    sts_v2(stg + off, make_uint2(__byte_perm(a, rr, sel_w0), __byte_perm(b, rr, sel_w1)));
                             }
                         }
                         fence_proxy_async_shared();
                         __syncwarp();
-                        if (lane == 0) {
+                        if (lane == 0 && FP8_IN_BOUNDS(wrow0 + 32 <= p.M && n0 + 64 * c + 64 <= p.N)) {
                             tma_store_2d(&tmC, stg, n0 + 64 * c, wrow0);
                             bulk_commit_group();
                         }
@@ -628,9 +630,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint2 lo = quant8_bf16(make_uint4(w[8 * c], w[8 * c + 1], w[8 * c + 2], w[8 * c + 3]), gs);
                     const uint2 hi =
                         quant8_bf16(make_uint4(w[8 * c + 4], w[8 * c + 5], w[8 * c + 6], w[8 * c + 7]), gs);
-                    stg_v4(qrow + 16 * c, make_uint4(lo.x, lo.y, hi.x, hi.y));
+                    if (FP8_IN_BOUNDS(grow < p.M && n0 + 16 * c + 16 <= p.N))
+                        stg_v4(qrow + 16 * c, make_uint4(lo.x, lo.y, hi.x, hi.y));
                 }
-                qo.sC[static_cast<int64_t>(grow) * qo.sc_m + static_cast<int64_t>(n0 / 128) * qo.sc_nb] = gs.s;
+                if (FP8_IN_BOUNDS(grow < p.M && n0 < p.N))
+                    qo.sC[static_cast<int64_t>(grow) * qo.sc_m + static_cast<int64_t>(n0 / 128) * qo.sc_nb] = gs.s;
             } else {
                 // the warp's 32 rows x 128 columns in two 32 x 64 TMA stores: each lane
                 // writes its row into the swizzled staging tile (16-byte chunk j of row r
@@ -644,13 +648,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         const int o = 64 * h + 8 * j;
+                        if (FP8_IN_BOUNDS(lane * 128 + ((j ^ (lane & 7)) << 4) + 16 <= static_cast<int>(C_STAGE_BYTES)))
                         sts_v4(stg + lane * 128 + ((j ^ (lane & 7)) << 4),
                                make_uint4(pack_bf16x2(acc[o + 0], acc[o + 1]), pack_bf16x2(acc[o + 2], acc[o + 3]),
                                           pack_bf16x2(acc[o + 4], acc[o + 5]), pack_bf16x2(acc[o + 6], acc[o + 7])));
                     }
                     fence_proxy_async_shared();
                     __syncwarp();
-                    if (lane == 0) {
+                    if (lane == 0 && FP8_IN_BOUNDS(wrow0 + 32 <= tl.row_end && n0 + 64 * h + 64 <= p.N)) {
                         tma_store_2d(&tmC, stg, n0 + 64 * h, wrow0);
                         bulk_commit_group();
                     }

@@ -393,7 +393,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 break;
             }
             if (is_a) {
-                sts_v4(sm_sfa + sslot * SFA_BYTES + 16 * lane, make_uint4(word(0, 0), word(0, 1), word(0, 2), word(0, 3)));
+                if (FP8_IN_BOUNDS(sslot < SF_SLOTS))
+                    sts_v4(sm_sfa + sslot * SFA_BYTES + 16 * lane, make_uint4(word(0, 0), word(0, 1), word(0, 2), word(0, 3)));
             } else {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     } else {
                         w4 = make_uint4(word(h, 0), word(h, 1), word(h, 2), word(h, 3));
                     }
-                    sts_v4(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane, w4);
+                    if (FP8_IN_BOUNDS(sslot < SF_SLOTS)) sts_v4(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane, w4);
                 }
             }
             fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
@@ -457,7 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     w.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
                     w.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
                     w.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-                    stg_v4(crow + c0 + 8 * j, w);
+                    if (FP8_IN_BOUNDS(grow < tl.row_end && n0 + c0 + 8 * j + 8 <= p.N)) stg_v4(crow + c0 + 8 * j, w);
                 }
             };
             store32(r0, 0);

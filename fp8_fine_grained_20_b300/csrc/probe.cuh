@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(128, 1) k_mma_accumulation_probe(const __grid_
         tmem_ld_32cols(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, r);
         tmem_wait_ld(r);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) out[static_cast<int64_t>(row) * BN + c + j] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j)
+            if (FP8_IN_BOUNDS(row < BM && c + j < BN)) out[static_cast<int64_t>(row) * BN + c + j] = __uint_as_float(r[j]);
     }
     tc_fence_before_sync();
     __syncthreads();

@@ -21,6 +21,7 @@ constexpr uint32_t kWaitMaxPolls = 1u << 30;
 // Status codes recorded on the device (values of fp8_status_t).
 constexpr int kStatusTimeout = 5;
 constexpr int kStatusBadGroups = 8;
+constexpr int kStatusBounds = 10;
 
 // One status word per device; the first error recorded wins.
 __device__ int g_fp8_device_status;
@@ -28,6 +29,22 @@ __device__ int g_fp8_device_status;
 __device__ __forceinline__ void record_status(int code) {
     atomicCAS(&g_fp8_device_status, 0, code);
 }
+
+// Bounds-checked build (-DFP8FG_BOUNDS): every device write of the kernels is
+// guarded by FP8_IN_BOUNDS(condition), the condition stating that the write
+// stays inside its tensor's logical extent (or its shared-memory tile).  A
+// write that would not is skipped and FP8_ERR_DEVICE_BOUNDS is recorded in the
+// status word.  In the normal build the macro is `true` and the condition is
+// not evaluated.
+#ifdef FP8FG_BOUNDS
+__device__ __forceinline__ bool bounds_ok(bool ok) {
+    if (!ok) record_status(kStatusBounds);
+    return ok;
+}
+#define FP8_IN_BOUNDS(cond) (::fp8fg::bounds_ok(cond))
+#else
+#define FP8_IN_BOUNDS(cond) (true)
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

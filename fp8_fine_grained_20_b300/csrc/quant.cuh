@@ -292,8 +292,11 @@ __global__ void __launch_bounds__(256) k_quant_act_1x128(const uint16_t* __restr
                 const GroupScale g = group_scale_t<POW2>(a);
                 uint8_t* dst = q + static_cast<int64_t>(mu[u]) * ldq + kbu[u] * 128 + sub * 8;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) stg_v2(dst + 32 * i, quant8_bf16<POW2>(v[u][i], g));
-                if (sub == 0) s[static_cast<int64_t>(mu[u]) * ssm + static_cast<int64_t>(kbu[u]) * sskb] = g.s;
+                for (int i = 0; i < 4; ++i)
+                    if (FP8_IN_BOUNDS(kbu[u] * 128 + sub * 8 + 32 * i + 8 <= KB * 128))
+                        stg_v2(dst + 32 * i, quant8_bf16<POW2>(v[u][i], g));
+                if (sub == 0 && FP8_IN_BOUNDS(mu[u] < M && kbu[u] < KB))
+                    s[static_cast<int64_t>(mu[u]) * ssm + static_cast<int64_t>(kbu[u]) * sskb] = g.s;
             }
         }
     }
@@ -415,7 +418,7 @@ __global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_
 #pragma unroll
         for (int k = 1; k < 8; ++k) am = fmaxf(am, red[k]);
         const GroupScale gs = group_scale_t<POW2>(am);
-        if (tid == 0)
+        if (tid == 0 && FP8_IN_BOUNDS(g < a.G && kb < a.KB && nb < a.NB))
             a.s[static_cast<int64_t>(g) * a.s_gstride + static_cast<int64_t>(kb) * a.sskb +
                 static_cast<int64_t>(nb) * a.ssnb] = gs.s;
 
@@ -426,20 +429,24 @@ __global__ void __launch_bounds__(WQ_THREADS, 2) k_quant_w_128x128(const __grid_
         if (!a.kmajor) {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                stg_v2(qg + static_cast<int64_t>(kb * 128 + 8 * rb + j) * a.ldq + nb * 128 + 8 * nc, rows[j]);
+                if (FP8_IN_BOUNDS(kb * 128 + 8 * rb + j < a.KB * 128 && nb * 128 + 8 * nc + 8 <= a.NB * 128))
+                    stg_v2(qg + static_cast<int64_t>(kb * 128 + 8 * rb + j) * a.ldq + nb * 128 + 8 * nc, rows[j]);
             __syncthreads();   // B: red[] may be rewritten by the next block
         } else {
             uint2 cols[8];
             transpose8x8(rows, cols);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) sts_v2(out + stage_row<3>(8 * nc + j) + 8 * rb, cols[j]);
+            for (int j = 0; j < 8; ++j)
+                if (FP8_IN_BOUNDS(stage_row<3>(8 * nc + j) + 8 * rb + 8 <= WQ_STAGE_OUT))
+                    sts_v2(out + stage_row<3>(8 * nc + j) + 8 * rb, cols[j]);
             __syncthreads();   // B: the staged tile is complete
             uint8_t* dst = qg + static_cast<int64_t>(nb * 128) * a.ldq + kb * 128;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int id = tid + WQ_THREADS * u;    // 128 rows x 8 chunks of 16 bytes
                 const int row = id >> 3, ch = id & 7;
-                stg_v4(dst + static_cast<int64_t>(row) * a.ldq + 16 * ch, lds_v4(out + stage_row<3>(row) + 16 * ch));
+                if (FP8_IN_BOUNDS(nb * 128 + row < a.NB * 128 && kb * 128 + 16 * ch + 16 <= a.KB * 128))
+                    stg_v4(dst + static_cast<int64_t>(row) * a.ldq + 16 * ch, lds_v4(out + stage_row<3>(row) + 16 * ch));
             }
         }
     }
@@ -619,7 +626,7 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
         am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 8));
         am1 = fmaxf(am1, __shfl_xor_sync(0xffffffffu, am1, 16));
         const GroupScale gs = group_scale_t<POW2>((g & 1) ? am1 : am0);   // lane (g, c): channel 2c + (g & 1)
-        if (g < 2)
+        if (g < 2 && FP8_IN_BOUNDS(kb * 128 + 16 * w + 2 * c + g < a.KB * 128 && mb < a.MB))
             a.sT[static_cast<int64_t>(kb * 128 + 16 * w + 2 * c + g) * a.sTk + static_cast<int64_t>(mb) * a.sTmb] =
                 gs.s;
         float chs[2], chr[2];
@@ -646,14 +653,16 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
                 for (int aa = 0; aa < 16; ++aa) {
                     const uint32_t code =
                         e4m3_pair(div2_neg_t<POW2>(make_float2(xv[aa][j], xv[aa][2 + j]), nr2, s2));
-                    sts_u16_at((ob ^ static_cast<uint32_t>((aa >> 1) << 4)) + 8 * (aa & 1), code);
+                    const uint32_t at = (ob ^ static_cast<uint32_t>((aa >> 1) << 4)) + 8 * (aa & 1);
+                    if (FP8_IN_BOUNDS(at >= smem_addr(wst) && at + 2 <= smem_addr(wst) + RQ_WSTAGE)) sts_u16_at(at, code);
                 }
             } else {
 #pragma unroll
                 for (int aa = 0; aa < 16; ++aa) {
                     const uint32_t code = quant_div(-xv[aa][j], chs[j], chm[j]) |
                                           (quant_div(-xv[aa][2 + j], chs[j], chm[j]) << 8);
-                    sts_u16_at((ob ^ static_cast<uint32_t>((aa >> 1) << 4)) + 8 * (aa & 1), code);
+                    const uint32_t at = (ob ^ static_cast<uint32_t>((aa >> 1) << 4)) + 8 * (aa & 1);
+                    if (FP8_IN_BOUNDS(at >= smem_addr(wst) && at + 2 <= smem_addr(wst) + RQ_WSTAGE)) sts_u16_at(at, code);
                 }
             }
         }
@@ -663,7 +672,8 @@ __global__ void __launch_bounds__(RQ_THREADS, 2) k_requant_1x128_to_128x1(const 
         for (int u = 0; u < 4; ++u) {
             const int id = lane + 32 * u;    // 16 rows x 8 chunks of 16 bytes
             const int row = id >> 3, ch = id & 7;
-            stg_v4(dst + static_cast<int64_t>(row) * a.ldqT + 16 * ch, lds_v4(wst + row * 128 + ((ch ^ (row >> 1)) << 4)));
+            if (FP8_IN_BOUNDS(kb * 128 + 16 * w + row < a.KB * 128 && mb * 128 + 16 * ch + 16 <= a.MB * 128))
+                stg_v4(dst + static_cast<int64_t>(row) * a.ldqT + 16 * ch, lds_v4(wst + row * 128 + ((ch ^ (row >> 1)) << 4)));
         }
         __syncwarp();
     }

@@ -127,13 +127,16 @@ __global__ void __launch_bounds__(256) k_swiglu_quant_1x128(const SwigluArgs a) 
                 const int64_t col = static_cast<int64_t>(fbu[u]) * 128 + sub * 8;
                 uint8_t* dst = a.q + static_cast<int64_t>(mu[u]) * a.ldq + col;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) stg_v2(dst + 32 * i, quant8_bf16(yv[i], gsc));
-                if (sub == 0)
+                for (int i = 0; i < 4; ++i)
+                    if (FP8_IN_BOUNDS(col + 32 * i + 8 <= static_cast<int64_t>(a.FB) * 128))
+                        stg_v2(dst + 32 * i, quant8_bf16(yv[i], gsc));
+                if (sub == 0 && FP8_IN_BOUNDS(mu[u] < a.M && fbu[u] < a.FB))
                     a.s[static_cast<int64_t>(mu[u]) * a.ssm + static_cast<int64_t>(fbu[u]) * a.ssfb] = gsc.s;
                 if (a.y != nullptr) {
                     uint16_t* yd = a.y + static_cast<int64_t>(mu[u]) * a.ldy + col;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) stg_v4(yd + 32 * i, yv[i]);
+                    for (int i = 0; i < 4; ++i)
+                        if (FP8_IN_BOUNDS(col + 32 * i + 8 <= static_cast<int64_t>(a.FB) * 128)) stg_v4(yd + 32 * i, yv[i]);
                 }
             }
         }

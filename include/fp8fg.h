@@ -65,7 +65,9 @@ typedef enum fp8_status {
     FP8_ERR_ARG = 6,             /* an enum or stride argument is invalid */
     FP8_ERR_DEVICE = 7,          /* the current device is not sm_103 / lacks resources */
     FP8_ERR_DEVICE_GROUPS = 8,   /* (device status) group offsets were not valid */
-    FP8_ERR_DEVICE_SCALES = 9    /* (device status) a scale given to an _mx GEMM is not a power of two */
+    FP8_ERR_DEVICE_SCALES = 9,   /* (device status) a scale given to an _mx GEMM is not a power of two */
+    FP8_ERR_DEVICE_BOUNDS = 10   /* (device status, bounds-checked debug build only) a device write fell
+                                    outside its tensor or shared-memory tile and was skipped */
 } fp8_status_t;
 
 /* Layout of the codes written by fp8_quant_w_128x128. */

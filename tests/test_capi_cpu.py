@@ -232,3 +232,14 @@ def test_swiglu_quant_rejections(lib):
     assert f(*bad) == 6                                   # ldy < F with a y output
     bad = list(ok); bad[11] = MIS; bad[12] = 256
     assert f(*bad) == 2                                   # misaligned y
+
+
+def test_bounds_checked_build_exports_every_symbol():
+    """The debug build with every device write bounds-checked (-DFP8FG_BOUNDS,
+    loaded when FP8FG_BOUNDS=1) is the same C ABI."""
+    path = fgbuild.build(bounds=True)
+    dbg = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    dbg.fp8_status_string.restype = ctypes.c_char_p
+    assert dbg.fp8_status_string(10).decode().startswith("FP8_ERR_DEVICE_BOUNDS")
