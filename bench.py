@@ -356,7 +356,7 @@ def load_tensor_pipe():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("ptx.cuh", "quant.cuh", "gemm.cuh", "fp8fg.cu"):
+    for f in ("ptx.cuh", "quant.cuh", "gemm.cuh", "gemm_mx.cuh", "swiglu.cuh", "fp8fg.cu"):
         with open(os.path.join(ROOT, "fp8_fine_grained_20_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

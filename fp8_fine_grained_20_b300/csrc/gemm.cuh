@@ -120,14 +120,19 @@ struct Tile {
     int row0, nb, g, row_end;
 };
 
-// Pair-tile index -> (pair-row, n-block): GROUP_PM consecutive pair-rows share
+// Pair-tile index -> (pair-row, n-block): GROUP consecutive pair-rows share
 // each n-block before moving on, so concurrently running pairs reuse A and B
-// in L2.
+// in L2.  The grouped power-of-two GEMM, whose A streams from DRAM, uses
+// groups of 2 (each A row block is consumed by its n-blocks close together in
+// time: measured 7% faster than 8 on the MoE workload); the others use 8.
+// GROUP is a compile-time constant: a run-time group costs the promoting
+// forward GEMM's epilogue enough registers to spill (measured 2.3x slower).
+template <int GROUP>
 __device__ __forceinline__ void raster(int t, int pair_rows, int n_blocks, int& pr, int& nb) {
-    const int span = GROUP_PM * n_blocks;
+    const int span = GROUP * n_blocks;
     const int grp = t / span;
-    const int first = grp * GROUP_PM;
-    const int gm = min(GROUP_PM, pair_rows - first);
+    const int first = grp * GROUP;
+    const int gm = min(GROUP, pair_rows - first);
     const int r = t - grp * span;
     pr = first + r % gm;
     nb = r / gm;
@@ -145,11 +150,11 @@ __device__ __forceinline__ int expert_of_pair_row(int pr, const int* ppre, int G
     return lo;
 }
 
-template <bool GROUPED>
+template <bool GROUPED, int GROUP = GROUP_PM>
 __device__ __forceinline__ Tile tile_at(int t, const Args& p, int pair_rows, const int* goff, const int* ppre) {
     Tile x;
     int pr;
-    raster(t, pair_rows, p.n_blocks, pr, x.nb);
+    raster<GROUP>(t, pair_rows, p.n_blocks, pr, x.nb);
     if (!GROUPED) {
         x.g = 0;
         x.row0 = pr * PM;

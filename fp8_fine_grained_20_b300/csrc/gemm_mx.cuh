@@ -167,7 +167,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 
 // Launch: clusters of 2 CTAs along x, THREADS threads, MX_SMEM_PLAIN or
 // MX_SMEM_GROUPED bytes of dynamic shared memory, one CTA per SM.
-template <int SBK, bool GROUPED>
+template <int SBK, bool GROUPED, int MX_GROUP = GROUPED ? 2 : GROUP_PM>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args p) {
     extern __shared__ uint8_t smem_raw[];
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int t = pair; ok && t < num_tiles; t += n_pairs) {
-                const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+                const Tile tl = tile_at<GROUPED, MX_GROUP>(t, p, pair_rows, goff, ppre);
                 const int a_y = tl.row0 + static_cast<int>(rank) * BM;
                 const int b_y = tl.g * p.N + tl.nb * BN + static_cast<int>(rank) * BNH;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool is_a = warp == 2;
         float v[2][4][KB_PER_SF];   // A: [0][i][b] row lane + 32 i; B: [h][i][b] (block scales: i = 0 only)
         auto load = [&](int t, int gi) {
-            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            const Tile tl = tile_at<GROUPED, MX_GROUP>(t, p, pair_rows, goff, ppre);
             const int kb0 = gi * KB_PER_SF;
             const int nk = min(KB_PER_SF, p.k_blocks - kb0);
             if (is_a) {
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t tile_it = 0;
         for (int t = pair; t < num_tiles; t += n_pairs, ++tile_it) {
             // the tile's place, found while no accumulator values are live
-            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            const Tile tl = tile_at<GROUPED, MX_GROUP>(t, p, pair_rows, goff, ppre);
             const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
             const int n0 = tl.nb * BN + half * 128;
             const bool store = grow < tl.row_end && n0 < p.N;

@@ -150,9 +150,10 @@ __device__ __forceinline__ float2 div2_t(float2 x, float2 r2, float2 ns2) {
 template <bool POW2>
 __device__ __forceinline__ float2 div2_neg_t(float2 nx, float2 nr2, float2 s2) {
     float2 q = __fmul2_rn(nx, nr2);
-    if (POW2) return q;
+    if constexpr (!POW2) {
 #pragma unroll
-    for (int i = 0; i < 2; ++i) q = __ffma2_rn(__ffma2_rn(q, s2, nx), nr2, q);
+        for (int i = 0; i < 2; ++i) q = __ffma2_rn(__ffma2_rn(q, s2, nx), nr2, q);
+    }
     return q;
 }
 
