@@ -212,7 +212,7 @@ fp8_status_t launch_gemm_mx(const uint8_t* A, int64_t lda, int64_t a_rows, const
     auto kernel = gemm::k_gemm_mx<SBK, GROUPED>;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    const fp8_status_t rc = pair_config(kernel, GROUPED ? gemm::MX_SMEM_GROUPED : gemm::MX_SMEM_PLAIN, st, args,
+    const fp8_status_t rc = pair_config(kernel, gemm::mx_smem(SBK, GROUPED), st, args,
                                         GROUPED, stream, cfg, attr);
     if (rc != FP8_OK) return rc;
     CUtensorMap tmA, tmB;

@@ -53,7 +53,7 @@ namespace fp8fg {
 namespace gemm {
 
 constexpr int MX_STAGES = 6;
-constexpr int SF_SLOTS = 3;                 // groups of four K-blocks in flight
+constexpr int SF_SLOTS = 6;                 // groups of four K-blocks in flight (TMEM scale slots)
 constexpr int KB_PER_SF = 4;                // K-blocks per scale word (bytes 0..3)
 constexpr uint32_t SFA_BYTES = 512;         // one atom: 128 rows x 4 bytes
 constexpr uint32_t SFB_BYTES = 1024;        // two atoms: 256 columns x 4 bytes
@@ -66,13 +66,30 @@ constexpr size_t MX_OFF_B = MX_OFF_A + MX_STAGES * A_BYTES;
 constexpr size_t MX_OFF_SFA = MX_OFF_B + MX_STAGES * B_BYTES;
 constexpr size_t MX_OFF_SFB = MX_OFF_SFA + SF_SLOTS * SFA_BYTES;
 constexpr size_t MX_OFF_BAR = MX_OFF_SFB + SF_SLOTS * SFB_BYTES;
-constexpr int MX_N_BARS = 2 * MX_STAGES + 2 * SF_SLOTS + 3;
+constexpr int MX_N_BARS = 2 * MX_STAGES + 2 * SF_SLOTS + 3 + 2 * 4;   // + rawfull / rawempty of the SF_RAW ring
 constexpr size_t MX_OFF_MISC = MX_OFF_BAR + MX_N_BARS * sizeof(uint64_t);
 constexpr size_t MX_OFF_GOFF = MX_OFF_MISC + 16;
-constexpr size_t MX_SMEM_PLAIN = 1024 + MX_OFF_GOFF;
-constexpr size_t MX_SMEM_GROUPED = 1024 + MX_OFF_GOFF + 2 * (MAX_GROUPS + 1) * sizeof(int);
+
+// The fp32 scales are copied (cp.async, warp 3) into a ring of SF_RAW groups,
+// so that several groups' global loads are in flight while the MMAs consume
+// the current one; warp 2 converts each group to UE8M0 atoms.  A slot holds
+// [value 4 w + b][lane]: w the lane's scale word (A: 4 rows; B: 2 halves x 4
+// columns, or 2 halves for per-block scales), b its K-block.  The ring
+// follows the expert offsets of the grouped kernel.
+constexpr int SF_RAW = 4;
+static_assert(MX_N_BARS == 2 * MX_STAGES + 2 * SF_SLOTS + 3 + 2 * SF_RAW, "barrier count");
+constexpr uint32_t RAWA_BYTES = 16 * 32 * 4;
+__host__ __device__ constexpr uint32_t mx_rawb_bytes(int sbk) { return (sbk == SB_BLOCK ? 8u : 32u) * 32u * 4u; }
+__host__ __device__ constexpr size_t mx_off_rawa(bool grouped) {
+    return (MX_OFF_GOFF + (grouped ? 2 * (MAX_GROUPS + 1) * sizeof(int) : 0) + 127) & ~size_t(127);
+}
+__host__ __device__ constexpr size_t mx_off_rawb(bool grouped) { return mx_off_rawa(grouped) + SF_RAW * RAWA_BYTES; }
+// dynamic shared memory of a launch (1024 bytes of alignment slack included)
+__host__ __device__ constexpr size_t mx_smem(int sbk, bool grouped) {
+    return 1024 + mx_off_rawb(grouped) + SF_RAW * mx_rawb_bytes(sbk);
+}
 static_assert(SF_TMEM_COL0 + SF_SLOTS * SF_TMEM_SLOT <= TMEM_COLS, "tensor memory budget");
-static_assert(MX_SMEM_GROUPED <= 227 * 1024, "shared memory budget");
+static_assert(mx_smem(SB_COL, false) <= 227 * 1024 && mx_smem(SB_BLOCK, true) <= 227 * 1024, "shared memory budget");
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4 with E4M3 A and B,
 // both K-major, UE8M0 scales: B scale byte (bits 4-5), A and B formats E4M3 (0),
@@ -184,6 +201,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint64_t* accfull = sfdone + SF_SLOTS;   // both: the tile's accumulator is complete
     uint64_t* accempty = accfull + 1;        // even CTA: both CTAs' epilogues hold the accumulator
     uint64_t* drain = accempty + 1;
+    uint64_t* rawfull = drain + 1;           // this CTA: the copier's fp32 scales of a ring slot landed
+    uint64_t* rawempty = rawfull + SF_RAW;   // this CTA: the converter has read a ring slot
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + MX_OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + MX_OFF_MISC + 4);
     int* groups_ok = reinterpret_cast<int*>(base + MX_OFF_MISC + 8);
@@ -202,8 +221,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&done[i], 1);
         }
         for (int i = 0; i < SF_SLOTS; ++i) {
-            mbar_init(&sfull[i], 4);    // two scale-loader warps in each CTA
+            mbar_init(&sfull[i], 2);    // the converter warp of each CTA
             mbar_init(&sfdone[i], 1);
+        }
+        for (int i = 0; i < SF_RAW; ++i) {
+            mbar_init(&rawfull[i], 32);   // one cp.async arrival per copier lane
+            mbar_init(&rawempty[i], 1);
         }
         mbar_init(accfull, 1);
         mbar_init(accempty, 2 * PROMO_WARPS);
@@ -341,83 +364,117 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(drain, 0, nullptr, ok ? kWaitTimeoutNs : kDrainTimeoutNs);
         }
     } else if (warp == 2 || warp == 3) {
-        // ----------------------------------------------- scale loaders ----
-        // warp 2: the A atom (this CTA's 128 rows); warp 3: the two B atoms
-        // (the tile's 256 columns).  Each keeps the fp32 scales of the next
-        // group of four K-blocks in registers: they are loaded right after
-        // the current group is written, so their latency overlaps the MMAs.
-        const bool is_a = warp == 2;
-        float v[2][4][KB_PER_SF];   // A: [0][i][b] row lane + 32 i; B: [h][i][b] (block scales: i = 0 only)
-        auto load = [&](int t, int gi) {
-            const Tile tl = tile_at<GROUPED, MX_GROUP>(t, p, pair_rows, goff, ppre);
-            const int kb0 = gi * KB_PER_SF;
-            const int nk = min(KB_PER_SF, p.k_blocks - kb0);
-            if (is_a) {
+        // ------------------------------------- scale copier and converter ----
+        // Group q of this pair's scale sequence (tile by tile, four K-blocks per
+        // group) goes through ring slot q % SF_RAW: warp 3 copies this CTA's A
+        // scales (its 128 rows) and the tile's B scales (256 columns) with
+        // cp.async, completing on rawfull; warp 2 converts them to the UE8M0
+        // atoms of TMEM scale slot q % SF_SLOTS.  The converter has no copies
+        // of its own in flight, so its proxy fence before publishing an atom
+        // does not wait for the prefetches.
+        const int ra_stride = static_cast<int>(RAWA_BYTES / sizeof(float));
+        const int rb_stride = static_cast<int>(mx_rawb_bytes(SBK) / sizeof(float));
+        float* raw_a = reinterpret_cast<float*>(base + mx_off_rawa(GROUPED)) + lane;
+        float* raw_b = reinterpret_cast<float*>(base + mx_off_rawb(GROUPED)) + lane;
+        const int total_groups = (num_tiles > pair) ? ((num_tiles - 1 - pair) / n_pairs + 1) * groups_per_tile : 0;
+        if (warp == 3) {
+            int it_t = pair, it_g = 0;
+            for (int q = 0; q < total_groups; ++q) {
+                const int slot = q % SF_RAW;
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(&rawempty[slot], ((q / SF_RAW) & 1) ^ 1, abort_flag, p.wait_ns))) {
+                    if (lane == 0) signal_abort(abort_flag, peer);
+                    break;
+                }
+                const Tile tl = tile_at<GROUPED, MX_GROUP>(it_t, p, pair_rows, goff, ppre);
+                const int kb0 = it_g * KB_PER_SF;
+                const int nk = min(KB_PER_SF, p.k_blocks - kb0);
                 const int r0 = tl.row0 + static_cast<int>(rank) * BM;
+                float* da = raw_a + slot * ra_stride;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int row = r0 + lane + 32 * i;
-                    const float* src = p.sA + static_cast<int64_t>(row) * p.sa_sm + static_cast<int64_t>(kb0) * p.sa_skb;
 #pragma unroll
-                    for (int b = 0; b < KB_PER_SF; ++b)
-                        v[0][i][b] = (row < p.M && b < nk) ? src[static_cast<int64_t>(b) * p.sa_skb] : 0.0f;
+                    for (int b = 0; b < KB_PER_SF; ++b) {
+                        const float* src = (row < p.M && b < nk) ? p.sA + static_cast<int64_t>(row) * p.sa_sm +
+                                                                       static_cast<int64_t>(kb0 + b) * p.sa_skb
+                                                                 : &g_zero_scale;
+                        cp_async_4(da + 32 * (4 * i + b), src);
+                    }
                 }
-            } else {
                 const float* sb_base = p.sB + static_cast<int64_t>(tl.g) * p.sb_group_stride;
+                float* db = raw_b + slot * rb_stride;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int i = 0; i < (SBK == SB_BLOCK ? 1 : 4); ++i) {
                         const int c = (SBK == SB_BLOCK) ? tl.nb * (BN / 128) + h : tl.nb * BN + 128 * h + lane + 32 * i;
-                        const float* src = sb_base + static_cast<int64_t>(kb0) * p.sb_skb + static_cast<int64_t>(c) * p.sb_sn;
 #pragma unroll
-                        for (int b = 0; b < KB_PER_SF; ++b)
-                            v[h][i][b] = (c < p.sb_cols && b < nk) ? src[static_cast<int64_t>(b) * p.sb_skb] : 0.0f;
+                        for (int b = 0; b < KB_PER_SF; ++b) {
+                            const float* src = (c < p.sb_cols && b < nk)
+                                                   ? sb_base + static_cast<int64_t>(kb0 + b) * p.sb_skb +
+                                                         static_cast<int64_t>(c) * p.sb_sn
+                                                   : &g_zero_scale;
+                            // value 4 (word) + b: word 4h + i (per column) or h (per block)
+                            cp_async_4(db + 32 * ((SBK == SB_BLOCK ? h : 4 * h + i) * 4 + b), src);
+                        }
                     }
-            }
-        };
-        bool bad = false;
-        auto word = [&](int h, int i) {
-            uint32_t w = 0;
-#pragma unroll
-            for (int b = 0; b < KB_PER_SF; ++b) w |= ue8m0_of(v[h][i][b], bad) << (8 * b);
-            return w;
-        };
-        const uint32_t sfull_even = mapa_shared(smem_addr(&sfull[0]), 0);
-        int t = pair, gi = 0;
-        if (t < num_tiles) load(t, gi);
-        for (uint32_t grp = 0; t < num_tiles; ++grp) {
-            const uint32_t sslot = grp % SF_SLOTS, sph = (grp / SF_SLOTS) & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns))) {
-                if (lane == 0) signal_abort(abort_flag, peer);
-                break;
-            }
-            if (is_a) {
-                if (FP8_IN_BOUNDS(sslot < SF_SLOTS))
-                    sts_v4(sm_sfa + sslot * SFA_BYTES + 16 * lane, make_uint4(word(0, 0), word(0, 1), word(0, 2), word(0, 3)));
-            } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint4 w4;
-                    if (SBK == SB_BLOCK) {
-                        const uint32_t w = word(h, 0);
-                        w4 = make_uint4(w, w, w, w);
-                    } else {
-                        w4 = make_uint4(word(h, 0), word(h, 1), word(h, 2), word(h, 3));
-                    }
-                    if (FP8_IN_BOUNDS(sslot < SF_SLOTS)) sts_v4(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane, w4);
+                cp_async_arrive_noinc(&rawfull[slot]);
+                if (++it_g == groups_per_tile) {
+                    it_g = 0;
+                    it_t += n_pairs;
                 }
             }
-            fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_release(sfull_even + sslot * sizeof(uint64_t));
-            if (++gi == groups_per_tile) {
-                gi = 0;
-                t += n_pairs;
+            asm volatile("cp.async.wait_all;" ::: "memory");
+        } else {
+            bool bad = false;
+            const uint32_t sfull_even = mapa_shared(smem_addr(&sfull[0]), 0);
+            for (int q = 0; q < total_groups; ++q) {
+                const int slot = q % SF_RAW;
+                if (!__all_sync(0xffffffffu, mbar_wait(&rawfull[slot], (q / SF_RAW) & 1, abort_flag, p.wait_ns))) {
+                    if (lane == 0) signal_abort(abort_flag, peer);
+                    break;
+                }
+                const float* va = raw_a + slot * ra_stride;
+                const float* vb = raw_b + slot * rb_stride;
+                uint32_t wa[4], wb[8];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t x = 0;
+#pragma unroll
+                    for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(va[32 * (4 * k + b)], bad) << (8 * b);
+                    wa[k] = x;
+                }
+#pragma unroll
+                for (int k = 0; k < (SBK == SB_BLOCK ? 2 : 8); ++k) {
+                    uint32_t x = 0;
+#pragma unroll
+                    for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(vb[32 * (4 * k + b)], bad) << (8 * b);
+                    wb[k] = x;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rawempty[slot]);   // the values are in registers
+                const uint32_t sslot = static_cast<uint32_t>(q) % SF_SLOTS;
+                const uint32_t sph = (static_cast<uint32_t>(q) / SF_SLOTS) & 1u;
+                if (!__all_sync(0xffffffffu, mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns))) {
+                    if (lane == 0) signal_abort(abort_flag, peer);
+                    break;
+                }
+                if (FP8_IN_BOUNDS(sslot < SF_SLOTS)) {
+                    sts_v4(sm_sfa + sslot * SFA_BYTES + 16 * lane, make_uint4(wa[0], wa[1], wa[2], wa[3]));
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 w4 = (SBK == SB_BLOCK) ? make_uint4(wb[h], wb[h], wb[h], wb[h])
+                                                           : make_uint4(wb[4 * h], wb[4 * h + 1], wb[4 * h + 2], wb[4 * h + 3]);
+                        sts_v4(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane, w4);
+                    }
+                }
+                fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_release(sfull_even + sslot * sizeof(uint64_t));
             }
-            if (t < num_tiles) load(t, gi);
+            if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(kStatusBadScale);
         }
-        if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(kStatusBadScale);
       }
     } else {
         regs_increase<208>();
