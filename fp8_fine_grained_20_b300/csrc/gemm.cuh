@@ -167,6 +167,27 @@ __device__ __forceinline__ Tile tile_at(int t, const Args& p, int pair_rows, con
     return x;
 }
 
+// While the current tile's last K-blocks stream in, the producer asks L2 for
+// the first PREFETCH_BLOCKS K-blocks of this CTA's boxes of its next tile, so
+// the next tile does not start on DRAM latency (the shared-memory ring holds
+// only the current tile's K-blocks at that point).
+constexpr int PREFETCH_AHEAD = 16;   // K-blocks before the end of a tile
+constexpr int PREFETCH_BLOCKS = 8;
+template <bool GROUPED, int GROUP = GROUP_PM>
+__device__ __noinline__ void prefetch_next_tile(int t, int num_tiles, const Args& p, int pair_rows, const int* goff,
+                                                   const int* ppre, uint32_t rank, const CUtensorMap* tmA,
+                                                   const CUtensorMap* tmB) {
+    if (t >= num_tiles) return;
+    const Tile tl = tile_at<GROUPED, GROUP>(t, p, pair_rows, goff, ppre);
+    const int a_y = tl.row0 + static_cast<int>(rank) * BM;
+    const int b_y = tl.g * p.N + tl.nb * BN + static_cast<int>(rank) * BNH;
+    const int n = min(PREFETCH_BLOCKS, p.k_blocks);
+    for (int kb = 0; kb < n; ++kb) {
+        tma_prefetch_l2_2d(tmA, kb * BK, a_y);
+        tma_prefetch_l2_2d(tmB, kb * BK, b_y);
+    }
+}
+
 
 template <int SBK, int OFF>
 __device__ __forceinline__ void promote32(float (&acc)[128], const uint32_t (&r)[32], float sc, float sa,
@@ -337,6 +358,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(&full[stage], STAGE_TX);
                     tma_load_2d_pair(sm_a + stage * A_BYTES, &tmA, fbar, kb * BK, a_y);
                     tma_load_2d_pair(sm_b + stage * B_BYTES, &tmB, fbar, kb * BK, b_y);
+                    if (kb == max(0, p.k_blocks - PREFETCH_AHEAD))
+                        prefetch_next_tile<GROUPED>(t + n_pairs, num_tiles, p, pair_rows, goff, ppre, rank, &tmA, &tmB);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;

@@ -291,6 +291,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (leader) mbar_arrive_expect_tx(&full[stage], STAGE_TX);
                     tma_load_2d_pair(sm_a + stage * A_BYTES, &tmA, fbar, kb * BK, a_y);
                     tma_load_2d_pair(sm_b + stage * B_BYTES, &tmB, fbar, kb * BK, b_y);
+                    if (kb == max(0, p.k_blocks - PREFETCH_AHEAD)) prefetch_next_tile<GROUPED, MX_GROUP>(
+                        t + n_pairs, num_tiles, p, pair_rows, goff, ppre, rank, &tmA, &tmB);
                     if (++stage == MX_STAGES) {
                         stage = 0;
                         phase ^= 1u;
