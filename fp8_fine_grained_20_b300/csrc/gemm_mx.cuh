@@ -146,6 +146,20 @@ __device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_add
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// The same with no ordering of this thread's earlier writes (see the
+// publication protocol of the scale converter).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Arrive on an mbarrier of this CTA with CTA-scope release, or relaxed.
+__device__ __forceinline__ void mbar_arrive_release_cta(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed_cta(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ void sts_u32(void* p, uint32_t v) {
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
@@ -317,8 +331,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (j == 0) {
                         // a new group: its scale atoms are in shared memory and the TMEM
                         // slot's previous group has finished its MMAs
-                        const bool ready = mbar_wait_cluster(&sfull[sslot], sph, abort_flag, p.wait_ns) &&
-                                           mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns);
+                        const bool ready = mbar_spin<true>(&sfull[sslot], sph, abort_flag, p.wait_ns) &&
+                                           mbar_spin(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns);
                         if (!__all_sync(0xffffffffu, ready)) {
                             if (lane == 0) signal_abort(abort_flag, peer);
                             ok = false;
@@ -332,8 +346,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                         __syncwarp();
                     }
-                    const bool ready = (kb != 0 || mbar_wait(accempty, (tile_it & 1u) ^ 1u, abort_flag, p.wait_ns)) &&
-                                       mbar_wait(&full[stage], phase, abort_flag, p.wait_ns);
+                    const bool ready = (kb != 0 || mbar_spin(accempty, (tile_it & 1u) ^ 1u, abort_flag, p.wait_ns)) &&
+                                       mbar_spin(&full[stage], phase, abort_flag, p.wait_ns);
                     if (!__all_sync(0xffffffffu, ready)) {
                         if (lane == 0) signal_abort(abort_flag, peer);
                         ok = false;
@@ -429,51 +443,87 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             asm volatile("cp.async.wait_all;" ::: "memory");
         } else {
+            // Groups are published two at a time: one release arrive (cluster
+            // scope from the odd CTA, whose atoms the even CTA's tcgen05.cp
+            // reads; CTA scope from the even CTA) orders the atoms of both, and
+            // the second group's arrive is relaxed.  The MMA warp acquires the
+            // first group's barrier before it waits on the second, so the second
+            // group's atoms are visible to it as well.  A cluster-scope release
+            // costs about 300 cycles on an idle B300 and over 1000 under this
+            // kernel's memory traffic; one per group made the converter slower
+            // than the MMAs.
             bool bad = false;
             const uint32_t sfull_even = mapa_shared(smem_addr(&sfull[0]), 0);
-            for (int q = 0; q < total_groups; ++q) {
-                const int slot = q % SF_RAW;
-                if (!__all_sync(0xffffffffu, mbar_wait(&rawfull[slot], (q / SF_RAW) & 1, abort_flag, p.wait_ns))) {
-                    if (lane == 0) signal_abort(abort_flag, peer);
-                    break;
-                }
-                const float* va = raw_a + slot * ra_stride;
-                const float* vb = raw_b + slot * rb_stride;
-                uint32_t wa[4], wb[8];
+            bool ok = true;
+            for (int q0 = 0; ok && q0 < total_groups; q0 += 2) {
+                const int nq = min(2, total_groups - q0);
+                uint32_t wa[2][4], wb[2][8];
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t x = 0;
-#pragma unroll
-                    for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(va[32 * (4 * k + b)], bad) << (8 * b);
-                    wa[k] = x;
-                }
-#pragma unroll
-                for (int k = 0; k < (SBK == SB_BLOCK ? 2 : 8); ++k) {
-                    uint32_t x = 0;
-#pragma unroll
-                    for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(vb[32 * (4 * k + b)], bad) << (8 * b);
-                    wb[k] = x;
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&rawempty[slot]);   // the values are in registers
-                const uint32_t sslot = static_cast<uint32_t>(q) % SF_SLOTS;
-                const uint32_t sph = (static_cast<uint32_t>(q) / SF_SLOTS) & 1u;
-                if (!__all_sync(0xffffffffu, mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns))) {
-                    if (lane == 0) signal_abort(abort_flag, peer);
-                    break;
-                }
-                if (FP8_IN_BOUNDS(sslot < SF_SLOTS)) {
-                    sts_v4(sm_sfa + sslot * SFA_BYTES + 16 * lane, make_uint4(wa[0], wa[1], wa[2], wa[3]));
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint4 w4 = (SBK == SB_BLOCK) ? make_uint4(wb[h], wb[h], wb[h], wb[h])
-                                                           : make_uint4(wb[4 * h], wb[4 * h + 1], wb[4 * h + 2], wb[4 * h + 3]);
-                        sts_v4(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane, w4);
+                for (int u = 0; u < 2; ++u) {
+                    if (u >= nq) break;
+                    const int q = q0 + u;
+                    const int slot = q % SF_RAW;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&rawfull[slot], (q / SF_RAW) & 1, abort_flag, p.wait_ns))) {
+                        ok = false;
+                        break;
                     }
+                    const float* va = raw_a + slot * ra_stride;
+                    const float* vb = raw_b + slot * rb_stride;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t x = 0;
+#pragma unroll
+                        for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(va[32 * (4 * k + b)], bad) << (8 * b);
+                        wa[u][k] = x;
+                    }
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        uint32_t x = 0;
+                        if (k < (SBK == SB_BLOCK ? 2 : 8)) {
+#pragma unroll
+                            for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(vb[32 * (4 * k + b)], bad) << (8 * b);
+                        }
+                        wb[u][k] = x;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&rawempty[slot]);   // the values are in registers
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    if (!ok || u >= nq) break;
+                    const uint32_t q = static_cast<uint32_t>(q0 + u);
+                    const uint32_t sslot = q % SF_SLOTS, sph = (q / SF_SLOTS) & 1u;
+                    if (!__all_sync(0xffffffffu, mbar_wait(&sfdone[sslot], sph ^ 1u, abort_flag, p.wait_ns))) {
+                        ok = false;
+                        break;
+                    }
+                    if (FP8_IN_BOUNDS(sslot < SF_SLOTS)) {
+                        sts_v4(sm_sfa + sslot * SFA_BYTES + 16 * lane, make_uint4(wa[u][0], wa[u][1], wa[u][2], wa[u][3]));
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 w4 = (SBK == SB_BLOCK)
+                                                 ? make_uint4(wb[u][h], wb[u][h], wb[u][h], wb[u][h])
+                                                 : make_uint4(wb[u][4 * h], wb[u][4 * h + 1], wb[u][4 * h + 2], wb[u][4 * h + 3]);
+                            sts_v4(sm_sfb + sslot * SFB_BYTES + 512 * h + 16 * lane, w4);
+                        }
+                    }
+                }
+                if (!ok) {
+                    if (lane == 0) signal_abort(abort_flag, peer);
+                    break;
                 }
                 fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster_release(sfull_even + sslot * sizeof(uint64_t));
+                if (lane == 0) {
+                    const uint32_t s0 = static_cast<uint32_t>(q0) % SF_SLOTS;
+                    if (rank == 0) {
+                        mbar_arrive_release_cta(&sfull[s0]);
+                        if (nq == 2) mbar_arrive_relaxed_cta(&sfull[(s0 + 1) % SF_SLOTS]);
+                    } else {
+                        mbar_arrive_cluster_release(sfull_even + s0 * sizeof(uint64_t));
+                        if (nq == 2) mbar_arrive_cluster_relaxed(sfull_even + ((s0 + 1) % SF_SLOTS) * sizeof(uint64_t));
+                    }
+                }
             }
             if (__any_sync(0xffffffffu, bad) && lane == 0) record_status(kStatusBadScale);
         }

@@ -108,6 +108,53 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     return false;
 }
 
+// Non-suspending variants for a thread on the critical issue path: the
+// phase is tested without a suspend-time hint, so the waiter notices a
+// completion by a remote (cluster) arrive at once instead of when the
+// suspended thread is next rescheduled.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Spin until the phase with the given parity completes, with the bounds of
+// mbar_wait; CLUSTER selects cluster-scope acquire.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_spin(uint64_t* bar, uint32_t parity, const volatile int* abort,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
+    const uint32_t a = smem_addr(bar);
+    auto test = [&]() { return CLUSTER ? mbar_test_wait_cluster(a, parity) : mbar_test_wait(a, parity); };
+    if (test()) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
+        if (test()) return true;
+        if ((i & 255u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (global_timer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+    return false;
+}
+
 // ------------------------------------------------------------- cluster ----
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
