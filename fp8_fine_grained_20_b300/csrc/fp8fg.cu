@@ -215,10 +215,11 @@ fp8_status_t launch_gemm_mx(const uint8_t* A, int64_t lda, int64_t a_rows, const
     const fp8_status_t rc = pair_config(kernel, gemm::mx_smem(SBK, GROUPED), st, args,
                                         GROUPED, stream, cfg, attr);
     if (rc != FP8_OK) return rc;
-    CUtensorMap tmA, tmB;
+    CUtensorMap tmA, tmB, tmC;
     if (!make_kmajor_map(&tmA, A, a_rows, args.K, lda, gemm::BM)) return FP8_ERR_CUDA;
     if (!make_kmajor_map(&tmB, B, b_rows, args.K, ldb, gemm::BNH)) return FP8_ERR_CUDA;
-    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, args) != cudaSuccess) {
+    if (!make_c_store_map(&tmC, args.C, args.M, args.N, args.ldc)) return FP8_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, args) != cudaSuccess) {
         cudaGetLastError();
         return FP8_ERR_CUDA;
     }

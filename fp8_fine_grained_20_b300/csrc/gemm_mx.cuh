@@ -52,7 +52,7 @@
 namespace fp8fg {
 namespace gemm {
 
-constexpr int MX_STAGES = 6;
+constexpr int MX_STAGES = 5;
 constexpr int SF_SLOTS = 6;                 // groups of four K-blocks in flight (TMEM scale slots)
 constexpr int KB_PER_SF = 4;                // K-blocks per scale word (bytes 0..3)
 constexpr uint32_t SFA_BYTES = 512;         // one atom: 128 rows x 4 bytes
@@ -63,7 +63,8 @@ constexpr int kStatusBadScale = 9;
 
 constexpr size_t MX_OFF_A = 0;
 constexpr size_t MX_OFF_B = MX_OFF_A + MX_STAGES * A_BYTES;
-constexpr size_t MX_OFF_SFA = MX_OFF_B + MX_STAGES * B_BYTES;
+constexpr size_t MX_OFF_C = MX_OFF_B + MX_STAGES * B_BYTES;   // per epilogue warp: a 32 x 64 bf16 staging tile
+constexpr size_t MX_OFF_SFA = MX_OFF_C + PROMO_WARPS * C_STAGE_BYTES;
 constexpr size_t MX_OFF_SFB = MX_OFF_SFA + SF_SLOTS * SFA_BYTES;
 constexpr size_t MX_OFF_BAR = MX_OFF_SFB + SF_SLOTS * SFB_BYTES;
 constexpr int MX_N_BARS = 2 * MX_STAGES + 2 * SF_SLOTS + 3 + 2 * 4;   // + rawfull / rawempty of the SF_RAW ring
@@ -200,11 +201,13 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 // MX_SMEM_GROUPED bytes of dynamic shared memory, one CTA per SM.
 template <int SBK, bool GROUPED, int MX_GROUP = GROUPED ? 2 : GROUP_PM>
 __global__ void __launch_bounds__(THREADS, 1)
-    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const Args p) {
+    k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmC, const Args p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sm_a = base + MX_OFF_A;
     uint8_t* sm_b = base + MX_OFF_B;
+    uint8_t* sm_c = base + MX_OFF_C;
     uint8_t* sm_sfa = base + MX_OFF_SFA;
     uint8_t* sm_sfb = base + MX_OFF_SFB;
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + MX_OFF_BAR);
@@ -533,14 +536,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ epilogue ----
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
-        const int row = quarter * 32 + lane;
         uint32_t tile_it = 0;
         for (int t = pair; t < num_tiles; t += n_pairs, ++tile_it) {
             // the tile's place, found while no accumulator values are live
             const Tile tl = tile_at<GROUPED, MX_GROUP>(t, p, pair_rows, goff, ppre);
-            const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
             const int n0 = tl.nb * BN + half * 128;
-            const bool store = grow < tl.row_end && n0 < p.N;
             if (!__all_sync(0xffffffffu, mbar_wait(accfull, tile_it & 1u, abort_flag, p.wait_ns))) {
                 if (lane == 0) signal_abort(abort_flag, peer);
                 break;
@@ -557,24 +557,43 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(accempty), 0));   // the even CTA's
-            if (!store) continue;
-            uint16_t* crow = p.C + static_cast<int64_t>(grow) * p.ldc + n0;
-            auto store32 = [&](const uint32_t (&r)[32], int c0) {
+            // the warp's 32 rows x 128 columns as bf16 in two 32 x 64 TMA stores: each
+            // lane writes its row into the warp's 128-byte-swizzled staging tile
+            // (16-byte chunk j of row r at chunk j ^ (r % 8)), then lane 0 issues the
+            // store; plain per-thread global stores here filled the memory pipeline
+            // that the MMA warp's barrier tests and copies also go through
+            uint8_t* stg = sm_c + (warp - 4) * C_STAGE_BYTES;
+            const int wrow0 = tl.row0 + static_cast<int>(rank) * BM + quarter * 32;
+            const bool wstore = wrow0 + 32 <= tl.row_end;   // 128-row blocks: whole warps are in or out
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(r[8 * j + 0]), __uint_as_float(r[8 * j + 1]));
-                    w.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3]));
-                    w.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5]));
-                    w.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7]));
-                    if (FP8_IN_BOUNDS(grow < tl.row_end && n0 + c0 + 8 * j + 8 <= p.N)) stg_v4(crow + c0 + 8 * j, w);
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t(&ra)[32] = h ? r2 : r0;
+                const uint32_t(&rb)[32] = h ? r3 : r1;
+                if (lane == 0) bulk_wait_read_all();   // the previous store has read the tile
+                __syncwarp();
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) {
+                    const uint32_t(&r)[32] = (jj < 4) ? ra : rb;
+                    const int o = 8 * (jj & 3);
+                    if (FP8_IN_BOUNDS(lane * 128 + ((jj ^ (lane & 7)) << 4) + 16 <= static_cast<int>(C_STAGE_BYTES)))
+                        sts_v4(stg + lane * 128 + ((jj ^ (lane & 7)) << 4),
+                               make_uint4(pack_bf16x2(__uint_as_float(r[o + 0]), __uint_as_float(r[o + 1])),
+                                          pack_bf16x2(__uint_as_float(r[o + 2]), __uint_as_float(r[o + 3])),
+                                          pack_bf16x2(__uint_as_float(r[o + 4]), __uint_as_float(r[o + 5])),
+                                          pack_bf16x2(__uint_as_float(r[o + 6]), __uint_as_float(r[o + 7]))));
                 }
-            };
-            store32(r0, 0);
-            store32(r1, 32);
-            store32(r2, 64);
-            store32(r3, 96);
+                fence_proxy_async_shared();
+                __syncwarp();
+                // N is a multiple of 128: a 64-column box is in or out as a whole
+                if (lane == 0 && wstore && n0 + 64 * h < p.N && FP8_IN_BOUNDS(n0 + 64 * h + 64 <= p.N)) {
+                    tma_store_2d(&tmC, stg, n0 + 64 * h, wrow0);
+                    bulk_commit_group();
+                }
+            }
         }
+        // every store of this warp has completed before its staging tile is released
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     // Teardown.  After the first cluster barrier no thread of either CTA waits
