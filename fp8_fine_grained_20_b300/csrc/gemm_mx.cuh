@@ -29,7 +29,8 @@
 //
 // Warp roles (384 threads, clusters of 2 CTAs, persistent over 256 x 256 pair
 // tiles in the grouped raster of gemm.cuh):
-//   warp 0 (both CTAs): TMA producer, as in k_gemm_blockscaled, STAGES-deep;
+//   warp 0 (both CTAs): TMA producer, as in k_gemm_blockscaled, MX_STAGES-deep,
+//     with the L2 prefetch of the next tile's first K-blocks;
 //   warp 1 (even CTA): MMA issuer -- per group of four K-blocks, three
 //     tcgen05.cp (A atom, two B atoms) into one of SF_SLOTS TMEM scale slots,
 //     then per K-block four block-scaled MMAs (K = 32 each, sf_id = the
@@ -37,14 +38,16 @@
 //     that frees the smem stage; after the group's last K-block a commit that
 //     frees the scale slot; after the tile's last K-block a commit that hands
 //     the accumulator to the epilogue;
-//   warps 2 and 3 (both CTAs): scale loaders (A, B) -- read the fp32 scales
-//     of a group of four K-blocks one group ahead, convert them to UE8M0
-//     bytes (the fp32 exponent field; any non-power-of-two scale sets
-//     FP8_ERR_DEVICE_SCALES) and write the atoms into a shared-memory slot;
+//   warp 3 (both CTAs): scale copier -- cp.async of the fp32 scales of this
+//     CTA's A rows and of the tile's B columns, SF_RAW groups ahead;
+//   warp 2 (both CTAs): scale converter -- UE8M0 bytes of those scales (the
+//     fp32 exponent field; any non-power-of-two scale sets
+//     FP8_ERR_DEVICE_SCALES) written as the atoms of a shared-memory slot,
+//     published two groups per release arrive;
 //   warps 4-11 (both CTAs): epilogue -- load the whole 128 x 256 FP32
 //     accumulator of this CTA into registers (128 values per thread), release
-//     it to the MMA issuer at once, then round to bf16 and store, overlapping
-//     the next tile's MMAs.
+//     it to the MMA issuer at once, then round to bf16 into swizzled staging
+//     tiles and store them with TMA, overlapping the next tile's MMAs.
 #pragma once
 
 #include "gemm.cuh"
@@ -161,44 +164,8 @@ __device__ __forceinline__ void mbar_arrive_relaxed_cta(uint64_t* bar) {
     asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-__device__ __forceinline__ void sts_u32(void* p, uint32_t v) {
-    asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Acquire-side wait at cluster scope (the releases come from both CTAs).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, 1000000;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const volatile int* abort,
-                                                  uint64_t timeout_ns) {
-    const uint32_t a = smem_addr(bar);
-    if (mbar_try_wait_cluster(a, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1; i < kWaitMaxPolls; ++i) {
-        if (mbar_try_wait_cluster(a, parity)) return true;
-        if ((i & 31u) == 0) {
-            if (abort != nullptr && *abort) return false;
-            if (global_timer_ns() - t0 > timeout_ns) return false;
-        }
-    }
-    return false;
-}
-
-// Launch: clusters of 2 CTAs along x, THREADS threads, MX_SMEM_PLAIN or
-// MX_SMEM_GROUPED bytes of dynamic shared memory, one CTA per SM.
+// Launch: clusters of 2 CTAs along x, THREADS threads, mx_smem(SBK, GROUPED)
+// bytes of dynamic shared memory, one CTA per SM.
 template <int SBK, bool GROUPED, int MX_GROUP = GROUPED ? 2 : GROUP_PM>
 __global__ void __launch_bounds__(THREADS, 1)
     k_gemm_mx(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -515,7 +482,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (lane == 0) signal_abort(abort_flag, peer);
                     break;
                 }
-                fence_proxy_async_smem();   // the atoms are read by tcgen05.cp (async proxy)
+                fence_proxy_async_shared();   // the atoms are read by tcgen05.cp (async proxy)
                 __syncwarp();
                 if (lane == 0) {
                     const uint32_t s0 = static_cast<uint32_t>(q0) % SF_SLOTS;

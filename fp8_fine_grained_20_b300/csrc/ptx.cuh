@@ -297,15 +297,6 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
-// Close this thread's current group of cp.async copies.
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
-// Wait until at most N of this thread's most recent cp.async groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // Arrive on `bar` once every cp.async this thread issued so far has landed;
 // the barrier's expected count must include this arrival (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
