@@ -376,6 +376,87 @@ def load_traffic():
     return t.get("bytes_per_launch", {})
 
 
+class NvmlClockSampler:
+    """Clock / throttle-reason / power samples every 5 ms from a background
+    thread through NVML (libnvidia-ml, the library nvidia-smi reads, called
+    through ctypes), so that even a timed region of a tenth of a second gets
+    tens of samples; only samples whose times fall inside the window given to
+    stop() are kept."""
+    INTERVAL_S = 0.005
+    CLOCK_SM = 1
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
+
+    def __init__(self, pci_bus_id):
+        import ctypes
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(pci_bus_id.encode()), ctypes.byref(self.h)) != 0:
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(0), ctypes.byref(self.h)) != 0:
+                raise RuntimeError("no NVML handle for %s" % pci_bus_id)
+        v = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetMaxClockInfo failed")
+        self.max_mhz = float(v.value)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.rows = []
+        self.stop_flag = None
+        self.thread = None
+
+    def _sample(self):
+        ct, lib = self.ct, self.lib
+        mhz, mw, bits = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ct.byref(mhz)) != 0 or
+                lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw)) != 0 or
+                self.reasons_fn(self.h, ct.byref(bits)) != 0):
+            return None
+        return (time.time(), float(mhz.value), mw.value / 1000.0,
+                {n for n, b in self.REASONS.items() if bits.value & b})
+
+    def _run(self):
+        while not self.stop_flag.is_set():
+            r = self._sample()
+            if r is not None:
+                self.rows.append(r)
+            self.stop_flag.wait(self.INTERVAL_S)
+
+    def start(self):
+        import threading
+        self.stop_flag = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self, t0=None, t1=None):
+        self.stop_flag.set()
+        self.thread.join(timeout=5)
+        inside = [r for r in self.rows if t0 is not None and t0 <= r[0] <= t1]
+        window = "timed region"
+        if not inside:
+            inside, window = self.rows, "whole sampling period (no sample inside the timed region)"
+        reasons = set()
+        for r in inside:
+            reasons |= r[3]
+        return {"sm_mhz": statistics.median(r[1] for r in inside) if inside else None,
+                "sm_max_mhz": self.max_mhz,
+                "power_w_median": statistics.median(r[2] for r in inside) if inside else None,
+                "samples": len(inside), "window": window, "interval_ms": 1000 * self.INTERVAL_S,
+                "source": "nvml", "reasons": sorted(reasons)}
+
+
+def clock_sampler(pci_bus_id):
+    """NVML sampler when the bindings and the device answer, else nvidia-smi."""
+    try:
+        return NvmlClockSampler(pci_bus_id)
+    except Exception as e:   # no bindings, no driver library, no such device
+        c = ClockSampler(pci_bus_id)
+        c.nvml_error = "%s: %s" % (type(e).__name__, e)
+        return c
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples (every 50 ms) while the timed
     region runs; only samples whose timestamps fall inside the window given to
@@ -446,7 +527,8 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(r[2] for r in inside) if inside else None,
                 "power_w_median": statistics.median(r[3] for r in inside) if inside else None,
-                "samples": len(inside), "window": window, "interval_ms": 50, "reasons": sorted(reasons)}
+                "samples": len(inside), "window": window, "interval_ms": 50, "source": "nvidia-smi",
+                "nvml_error": getattr(self, "nvml_error", None), "reasons": sorted(reasons)}
 
 
 # ------------------------------------------------------- CPU oracle leg ----
@@ -650,7 +732,7 @@ def main():
             for k in DeviceStep.KERNELS} for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(smi_id(torch, local))
+    clocks = clock_sampler(smi_id(torch, local))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -839,13 +921,13 @@ def run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, de
 
 def run_steady(args, step, stream, gpu, ms_step, world):
     """Run the step back to back for about args.steady_seconds with an event
-    pair around every step, sampling clocks every 50 ms.  Returns the median
-    step time, the clock record and step times grouped by the SM clock of the
-    nearest sample (100 MHz bins)."""
+    pair around every step, sampling clocks (every 5 ms through NVML, else
+    every 50 ms through nvidia-smi).  Returns the median, minimum and
+    last-quarter step times and the clock record of that run."""
     import torch
     n = max(10, int(args.steady_seconds * 1e3 / max(ms_step, 1e-3)))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
-    clocks = ClockSampler(gpu)
+    clocks = clock_sampler(gpu)
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
