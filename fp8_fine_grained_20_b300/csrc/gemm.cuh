@@ -20,7 +20,8 @@
 //     CTA, so every SM loads 32 KB per 128-deep K-block instead of 48 KB;
 //   * warp 0 (both CTAs): TMA producer -- this CTA's A box (128 x 128 B) and B
 //     half (128 x 128 B), 128-byte swizzle, 5-stage ring; the transaction
-//     bytes of both CTAs are counted on the even CTA's "full" barrier;
+//     bytes of both CTAs are counted on the even CTA's "full" barrier; near
+//     the end of each tile it asks L2 for the next tile's first K-blocks;
 //   * warp 1 (even CTA): MMA issuer (the whole warp runs the loop, one elected
 //     lane issues) -- per K-block, 4 x tcgen05.mma (K = 32)
 //     into one of two 256-column TMEM partial buffers, then one commit to the
@@ -33,7 +34,9 @@
 //     partial (each warp: its 32 TMEM lanes = rows, one 128-column half, in
 //     four 32-column loads, two in flight), release of the TMEM buffer to the
 //     even CTA as soon as the last two loads land, acc += partial * sA * sB in
-//     FP32 registers with packed FP32x2 FMAs, bf16 stores at tile end.  With
+//     FP32 registers with packed FP32x2 FMAs; at tile end bf16 through
+//     swizzled shared-memory staging tiles and TMA stores (or the 1x128
+//     codes and scales of the quantizing epilogue).  With
 //     per-column B scales (weight gradient) the loads use the 16x128b shape
 //     instead, so that a thread holds one column in four of four rows and
 //     reads 32 column scales per K-block rather than all 128 of its half.
