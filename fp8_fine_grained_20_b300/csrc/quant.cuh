@@ -16,12 +16,13 @@
 // Markstein's correction (P. Markstein, "Computation of elementary functions
 // on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): if r
 // is within half an ulp of 1/s and q is within one ulp of x/s, the remainder
-// e = x - q s is exact in one FMA and RN(q + e r) is RN(x/s).  q0 = RN(x r) can
-// be up to 1.5 ulps away, so two correction steps are applied (the first one
-// makes the value faithful, the second one exact):
+// e = x - q s is exact in one FMA and RN(q + e r) is RN(x/s).  For an fp32
+// dividend q0 = RN(x r) can be up to 1.5 ulps away, so two correction steps
+// are applied (the first one makes the value faithful, the second one exact):
 //     q0 = x r;  q1 = q0 + (x - q0 s) r;  q = q1 + (x - q1 s) r
-// as packed FP32x2 multiplies/FMAs on pairs of elements, followed by one
-// E4M3x2 conversion (round to nearest even, saturating).  The sign bit of
+// For a bf16 dividend one step is exact (div2_markstein_bf16 below says why).
+// Both run as packed FP32x2 multiplies/FMAs on pairs of elements, followed by
+// one E4M3x2 conversion (round to nearest even, saturating).  The sign bit of
 // each input is OR-ed into its code, so -0 and negative values that round to
 // zero keep the sign.  Groups with amax == 0 give zero codes; groups whose
 // scale is below 2^-92 use IEEE division per element.
