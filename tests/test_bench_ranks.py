@@ -54,3 +54,23 @@ def test_max_over_ranks_single_process():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.max_over_ranks(3.5, 1, "cpu") == 3.5
+
+
+def test_clock_sampler_reports_its_source():
+    """The clock sampler takes NVML when the driver library answers and falls
+    back to nvidia-smi otherwise; either way stop() returns a record that says
+    which source it used and keeps only samples inside the given window."""
+    sys.path.insert(0, ROOT)
+    import time
+    import bench
+    c = bench.clock_sampler("00000000:00:00.0")
+    c.start()
+    t0 = time.time()
+    time.sleep(0.05)
+    t1 = time.time()
+    rec = c.stop(t0, t1)
+    assert isinstance(rec, dict) and "reasons" in rec
+    if isinstance(c, bench.NvmlClockSampler):
+        assert rec["source"] == "nvml" and rec["samples"] >= 1
+    else:
+        assert getattr(c, "nvml_error", None)          # why NVML was not used
