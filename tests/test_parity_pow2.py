@@ -335,6 +335,31 @@ def test_mx_grouped_small_with_empty_experts(orc):
         assert np.all(got[offsets[g] + counts[g]:offsets[g + 1]] == 0.0)
 
 
+def test_mx_grouped_all_experts_empty(orc):
+    """Every expert empty: no tile, no scale group (the copier and converter
+    warps have nothing to do) and the output is not written."""
+    gu.cuda_or_skip()
+    qa = np.zeros((128, 256), np.uint8)
+    sa = np.zeros((128, 2), np.float32)
+    qb = np.zeros((3, 256, 256), np.uint8)
+    sb = np.ones((3, 2, 2), np.float32)
+    out = torch.full((128, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+    fg.fp8_grouped_gemm_blockscaled_mx(gu.dev(qa), scales_dev(sa, "mn"), gu.dev(qb), gu.dev(sb),
+                                       gu.dev(np.zeros(4, np.int32)), out=out)
+    torch.cuda.synchronize()
+    assert bool((out == 7.0).all())
+    assert fg.fp8_get_device_status(reset=True) == 0
+
+
+def test_mx_grouped_bad_offsets_report_device_status(orc):
+    counts = [128, 128]
+    qa, sa, qb, sb, offsets = moe_pow2(orc, counts, N=256, K=128, seed=5)
+    bad = offsets.copy()
+    bad[1] = 100                                   # not a multiple of 128
+    run_grouped_mx(qa, sa, qb, sb, bad)
+    assert fg.fp8_get_device_status(reset=True) == 8
+
+
 # ----------------------------------------------------------- full workloads --
 
 def test_mx_forward_full_workload_sampled(orc, threads):
