@@ -405,7 +405,7 @@ fp8_status_t requant_entry(const uint8_t* q, int64_t M, int64_t K, int64_t ldq, 
     a.sTmb = sT_stride_mb;
     a.MB = static_cast<int>(MB);
     a.KB = static_cast<int>(KB);
-    const int64_t cap = 2 * static_cast<int64_t>(sms);
+    const int64_t cap = RQ_CTAS_PER_SM * static_cast<int64_t>(sms);
     const int grid = static_cast<int>(MB * KB < cap ? MB * KB : cap);
     k_requant_1x128_to_128x1<POW2><<<grid, RQ_THREADS, RQ_SMEM, as_stream(stream)>>>(tm, a);
     return launch_status();
