@@ -85,7 +85,10 @@ constexpr int N_BARS = 2 * STAGES + 2 + 2 * SSLOTS + 1;
 constexpr size_t OFF_MISC = OFF_BAR + N_BARS * sizeof(uint64_t);
 constexpr size_t OFF_GOFF = OFF_MISC + 16;
 constexpr size_t SMEM_PLAIN = 1024 + OFF_GOFF;
-constexpr size_t SMEM_GROUPED = 1024 + OFF_GOFF + 2 * (MAX_GROUPS + 1) * sizeof(int);
+// the grouped flavour's promotion warps park their tile's place here during
+// the K-loop (16 bytes per warp)
+constexpr size_t OFF_TSTASH = (OFF_GOFF + 2 * (MAX_GROUPS + 1) * sizeof(int) + 15) & ~size_t(15);
+constexpr size_t SMEM_GROUPED = 1024 + OFF_TSTASH + PROMO_WARPS * 16;
 
 struct Args {
     const float* sA;
@@ -474,9 +477,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // Registers of the promotion warps (setmaxnreg; the four other warps
         // drop to 56).  Measured on B300: the plain forward / data-gradient
         // flavour runs 7% faster with 184 than with 224 (the allocator then
-        // spills 32 bytes instead of 92); the weight-gradient, grouped and
-        // quantizing flavours are fastest with 224.
-        regs_increase<(SBK == SB_BLOCK && !GROUPED && !QOUT) ? 184 : 224>();
+        // spills 32 bytes instead of 92); the weight-gradient and quantizing
+        // flavours are fastest with 224, the grouped one (with its tile's
+        // place parked in shared memory, below) with 208.
+        regs_increase<GROUPED ? 208 : (SBK == SB_BLOCK && !QOUT) ? 184 : 224>();
         // ------------------------------------- promotion and epilogue ----
         const int quarter = warp & 3;           // TMEM lanes 32*quarter .. +31
         const int half = (warp - 4) >> 2;       // output columns half*128 .. +127
@@ -487,7 +491,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int t = pair; ok && t < num_tiles; t += n_pairs) {
             // the tile's place, found before the K-loop (the grouped search then runs
             // while few registers are live)
-            const Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            Tile tl = tile_at<GROUPED>(t, p, pair_rows, goff, ppre);
+            if constexpr (GROUPED) {
+                // parked in shared memory until the epilogue: held in registers
+                // across the K-loop it made the allocator spill inside the loop
+                // (ncu: about three local stores per warp and K-block); parked,
+                // the grouped GEMM runs 3-6% faster on B300
+                if (lane == 0)
+                    *reinterpret_cast<int4*>(base + OFF_TSTASH + 16 * (warp - 4)) =
+                        make_int4(tl.row0, tl.row_end, tl.nb, tl.g);
+                __syncwarp();
+            }
             float acc[128];
 #pragma unroll
             for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
@@ -561,6 +575,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (lane == 0) mbar_arrive(&sempty[slot]);
             }
             if (!ok) break;
+            if constexpr (GROUPED) {
+                const volatile int* ts = reinterpret_cast<const volatile int*>(base + OFF_TSTASH + 16 * (warp - 4));
+                tl.row0 = ts[0];
+                tl.row_end = ts[1];
+                tl.nb = ts[2];
+                tl.g = ts[3];
+            }
             const int grow = tl.row0 + static_cast<int>(rank) * BM + row;
             const int n0 = tl.nb * BN + half * 128;
             if constexpr (SBK == SB_COL) {
