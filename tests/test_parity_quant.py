@@ -331,6 +331,14 @@ def test_requant_padded_strides(orc):
     assert np.all(gu.host(qTbuf)[:, M:] == 0xAB), "write outside the code rows"
 
 
+@pytest.mark.parametrize("M,K", [(128 * 600, 128), (128, 128 * 700)])
+def test_requant_more_blocks_than_ctas_along_one_axis(orc, M, K):
+    """One channel block and 600 token blocks, or one token block and 700
+    channel blocks: the persistent CTAs (four per SM) take several blocks each,
+    stepping along a single axis of the block grid."""
+    check_requant(orc, synth.wgrad_tensor(4, 2, M, K))
+
+
 def test_requant_full_quantizer_workload(orc):
     x, _ = synth.activation(2, 8192, 7168)
     check_requant(orc, x)
