@@ -326,6 +326,10 @@ def load_peaks():
 # maximum SM clock).  Used only for the clock-scaled context fraction.
 NOMINAL_FP8_FLOP_PER_CLK = 148 * 8192 * 2
 
+# Nominal HBM3e bandwidth the quantizers are also quoted against ("about
+# 8 TB/s"); the roofline fraction itself uses the measured copy bandwidth.
+NOMINAL_HBM_GBS = 8000.0
+
 
 def choose_fp8_peak(ms_total, clk, burst, sustained):
     """The FP8 roofline denominator: the burst figure (cuBLAS bf16 timed alone,
@@ -780,7 +784,8 @@ def main():
                 d["ncu_tensor_pipe_active"] = pipes[k]
         else:
             gbs = qbytes[k] / (ms * 1e-3) / 1e9
-            d.update({"gbs": gbs, "frac_hbm": gbs / hbm, "bytes": qbytes[k]})
+            d.update({"gbs": gbs, "frac_hbm": gbs / hbm, "frac_hbm_nominal": gbs / NOMINAL_HBM_GBS,
+                      "bytes": qbytes[k]})
         kernels[k] = d
     dom = max(per_kernel_ms, key=per_kernel_ms.get)
     if dom in flops:
@@ -834,7 +839,7 @@ def main():
             "fp8_peak_tflops": {"used": fp8_peak, "rule": peak_rule, "sustained": fp8_peak_sustained,
                                 "burst": fp8_peak_burst, "nominal_at_median_clock": fp8_nominal,
                                 "source": peak_src},
-            "hbm_peak_gbs": hbm,
+            "hbm_peak_gbs": hbm, "hbm_nominal_gbs": NOMINAL_HBM_GBS,
             "cpu_baseline": cpu, "e2e": e2e, "steady_state": steady, "pow2_mx": pow2,
             "gpu_launches": DeviceStep.LAUNCHES_PER_STEP * args.steps,
             "clocks": clk, "device_status": status,
@@ -909,7 +914,7 @@ def run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, de
             d.update({"tflops": tf, "frac_fp8": tf / fp8_peak})
         else:
             gbs = qbytes[k] / (ms * 1e-3) / 1e9
-            d.update({"gbs": gbs, "frac_hbm": gbs / hbm})
+            d.update({"gbs": gbs, "frac_hbm": gbs / hbm, "frac_hbm_nominal": gbs / NOMINAL_HBM_GBS})
         kernels[k] = d
     status = step.fg.fp8_get_device_status(reset=True)
     return {"ms_per_step": ms_step, "value": world * sum(flops.values()) / (ms_step * 1e-3) / 1e12,
