@@ -781,7 +781,7 @@ def main():
             if fp8_nominal:
                 d["frac_fp8_nominal_at_clock"] = tf / fp8_nominal
             if k in pipes:
-                d["ncu_tensor_pipe_active"] = pipes[k]
+                d["ncu_tensor_pipe_active_pct"] = pipes[k]
         else:
             gbs = qbytes[k] / (ms * 1e-3) / 1e9
             d.update({"gbs": gbs, "frac_hbm": gbs / hbm, "frac_hbm_nominal": gbs / NOMINAL_HBM_GBS,
@@ -795,7 +795,8 @@ def main():
                     "peak_source": "%s bf16 x %.0f (nominal FP8/BF16 ratio), %s" % (peak_src, FP8_OVER_BF16,
                                                                                    peak_rule),
                     "frac_nominal_at_clock": (ach / fp8_nominal) if fp8_nominal else None,
-                    "frac_tensor_pipe": pipes.get(dom)}
+                    # ncu sm__pipe_tensor_cycles_active of the same kernel, as a fraction
+                    "frac_tensor_pipe": (pipes[dom] / 100.0) if dom in pipes else None}
     else:
         ach = qbytes[dom] / (per_kernel_ms[dom] * 1e-3) / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
