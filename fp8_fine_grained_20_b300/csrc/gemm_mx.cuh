@@ -77,9 +77,11 @@ constexpr size_t MX_OFF_GOFF = MX_OFF_MISC + 16;
 // The fp32 scales are copied (cp.async, warp 3) into a ring of SF_RAW groups,
 // so that several groups' global loads are in flight while the MMAs consume
 // the current one; warp 2 converts each group to UE8M0 atoms.  A slot holds
-// [value 4 w + b][lane]: w the lane's scale word (A: 4 rows; B: 2 halves x 4
-// columns, or 2 halves for per-block scales), b its K-block.  The ring
-// follows the expert offsets of the grouped kernel.
+// A as [K-block b][128 rows] and per-column B as [b][256 columns], so that
+// scales contiguous in global memory (stride 1 along the rows or columns, the
+// usual layout) are copied four at a time; per-block B scales are held as
+// [value 4 h + b][lane] (h the column half, every lane its own copy).  The
+// ring follows the expert offsets of the grouped kernel.
 constexpr int SF_RAW = 4;
 static_assert(MX_N_BARS == 2 * MX_STAGES + 2 * SF_SLOTS + 3 + 2 * SF_RAW, "barrier count");
 constexpr uint32_t RAWA_BYTES = 16 * 32 * 4;
@@ -141,6 +143,24 @@ __device__ __forceinline__ uint32_t ue8m0_of(float s, bool& bad) {
     const uint32_t e = u >> 23;
     bad |= !(((u & 0x7FFFFFu) == 0u && e < 255u) || u == 0x00400000u);
     return e & 0xFFu;
+}
+
+// The UE8M0 bytes of four scales v[0], v[stride], v[2 stride], v[3 stride]
+// (four K-blocks) as one word, byte b from v[b stride].  Instead of checking
+// each value, mm collects the mantissa bits and hh the sign bits and the carry
+// of adding one to the exponent (set for an exponent of 255): both stay zero
+// for zero and normal powers of two, and the caller runs ue8m0_of on the
+// values whenever either is not (which also admits 2^-127, 0x00400000).
+__device__ __forceinline__ uint32_t ue8m0_word(const float* v, int stride, uint32_t& mm, uint32_t& hh) {
+    uint32_t t[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const uint32_t u = __float_as_uint(v[b * stride]);
+        mm |= u & 0x7FFFFFu;
+        hh |= u | (u + 0x800000u);
+        t[b] = u << 1;   // exponent in the top byte
+    }
+    return __byte_perm(__byte_perm(t[0], t[1], 0x0073), __byte_perm(t[2], t[3], 0x0073), 0x5410);
 }
 
 // Arrive once on an mbarrier of this CTA or the peer with cluster-scope
@@ -360,10 +380,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         // does not wait for the prefetches.
         const int ra_stride = static_cast<int>(RAWA_BYTES / sizeof(float));
         const int rb_stride = static_cast<int>(mx_rawb_bytes(SBK) / sizeof(float));
-        float* raw_a = reinterpret_cast<float*>(base + mx_off_rawa(GROUPED)) + lane;
-        float* raw_b = reinterpret_cast<float*>(base + mx_off_rawb(GROUPED)) + lane;
+        float* raw_a = reinterpret_cast<float*>(base + mx_off_rawa(GROUPED));
+        float* raw_b = reinterpret_cast<float*>(base + mx_off_rawb(GROUPED));
         const int total_groups = (num_tiles > pair) ? ((num_tiles - 1 - pair) / n_pairs + 1) * groups_per_tile : 0;
         if (warp == 3) {
+            // four scales per 16-byte copy where they are contiguous and aligned
+            const bool vec_a = p.sa_sm == 1 && (p.sa_skb & 3) == 0 && (reinterpret_cast<uintptr_t>(p.sA) & 15u) == 0;
+            const bool vec_b = SBK == SB_COL && p.sb_sn == 1 && (p.sb_skb & 3) == 0 && (p.sb_group_stride & 3) == 0 &&
+                               (reinterpret_cast<uintptr_t>(p.sB) & 15u) == 0;
             int it_t = pair, it_g = 0;
             for (int q = 0; q < total_groups; ++q) {
                 const int slot = q % SF_RAW;
@@ -376,35 +400,80 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int kb0 = it_g * KB_PER_SF;
                 const int nk = min(KB_PER_SF, p.k_blocks - kb0);
                 const int r0 = tl.row0 + static_cast<int>(rank) * BM;
-                float* da = raw_a + slot * ra_stride;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int row = r0 + lane + 32 * i;
+                float* da = raw_a + slot * ra_stride;   // [b][128 rows]
+                if (vec_a) {
+                    const int row = r0 + 4 * lane;      // rows row .. row + 3 (all in or all out: M % 128 == 0)
 #pragma unroll
                     for (int b = 0; b < KB_PER_SF; ++b) {
-                        const float* src = (row < p.M && b < nk) ? p.sA + static_cast<int64_t>(row) * p.sa_sm +
-                                                                       static_cast<int64_t>(kb0 + b) * p.sa_skb
-                                                                 : &g_zero_scale;
-                        cp_async_4(da + 32 * (4 * i + b), src);
+                        float* dst = da + 128 * b + 4 * lane;
+                        if (row < p.M && b < nk) {
+                            cp_async_16(dst, p.sA + row + static_cast<int64_t>(kb0 + b) * p.sa_skb);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) cp_async_4(dst + e, &g_zero_scale);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int row = r0 + lane + 32 * i;
+#pragma unroll
+                        for (int b = 0; b < KB_PER_SF; ++b) {
+                            const float* src = (row < p.M && b < nk) ? p.sA + static_cast<int64_t>(row) * p.sa_sm +
+                                                                           static_cast<int64_t>(kb0 + b) * p.sa_skb
+                                                                     : &g_zero_scale;
+                            cp_async_4(da + 128 * b + lane + 32 * i, src);
+                        }
                     }
                 }
                 const float* sb_base = p.sB + static_cast<int64_t>(tl.g) * p.sb_group_stride;
                 float* db = raw_b + slot * rb_stride;
+                if constexpr (SBK == SB_BLOCK) {
+                    // [value 4 h + b][lane]: every lane copies the two block scales
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int i = 0; i < (SBK == SB_BLOCK ? 1 : 4); ++i) {
-                        const int c = (SBK == SB_BLOCK) ? tl.nb * (BN / 128) + h : tl.nb * BN + 128 * h + lane + 32 * i;
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = tl.nb * (BN / 128) + h;
 #pragma unroll
                         for (int b = 0; b < KB_PER_SF; ++b) {
                             const float* src = (c < p.sb_cols && b < nk)
                                                    ? sb_base + static_cast<int64_t>(kb0 + b) * p.sb_skb +
                                                          static_cast<int64_t>(c) * p.sb_sn
                                                    : &g_zero_scale;
-                            // value 4 (word) + b: word 4h + i (per column) or h (per block)
-                            cp_async_4(db + 32 * ((SBK == SB_BLOCK ? h : 4 * h + i) * 4 + b), src);
+                            cp_async_4(db + 32 * (4 * h + b) + lane, src);
                         }
                     }
+                } else if (vec_b) {
+                    // [b][256 columns], four columns per copy (all in or all out: N % 128 == 0)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int c = tl.nb * BN + 128 * h + 4 * lane;
+#pragma unroll
+                        for (int b = 0; b < KB_PER_SF; ++b) {
+                            float* dst = db + 256 * b + 128 * h + 4 * lane;
+                            if (c < p.sb_cols && b < nk) {
+                                cp_async_16(dst, sb_base + static_cast<int64_t>(kb0 + b) * p.sb_skb + c);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) cp_async_4(dst + e, &g_zero_scale);
+                            }
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int c = tl.nb * BN + 128 * h + lane + 32 * i;
+#pragma unroll
+                            for (int b = 0; b < KB_PER_SF; ++b) {
+                                const float* src = (c < p.sb_cols && b < nk)
+                                                       ? sb_base + static_cast<int64_t>(kb0 + b) * p.sb_skb +
+                                                             static_cast<int64_t>(c) * p.sb_sn
+                                                       : &g_zero_scale;
+                                cp_async_4(db + 256 * b + 128 * h + lane + 32 * i, src);
+                            }
+                        }
+                }
                 cp_async_arrive_noinc(&rawfull[slot]);
                 if (++it_g == groups_per_tile) {
                     it_g = 0;
@@ -437,23 +506,29 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    const float* va = raw_a + slot * ra_stride;
-                    const float* vb = raw_b + slot * rb_stride;
+                    const float* va = raw_a + slot * ra_stride + lane;   // rows lane + 32 k of K-block b at 128 b + 32 k
+                    const float* vb = raw_b + slot * rb_stride + lane;
+                    uint32_t mm = 0, hh = 0;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        uint32_t x = 0;
-#pragma unroll
-                        for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(va[32 * (4 * k + b)], bad) << (8 * b);
-                        wa[u][k] = x;
-                    }
+                    for (int k = 0; k < 4; ++k) wa[u][k] = ue8m0_word(va + 32 * k, 128, mm, hh);
 #pragma unroll
                     for (int k = 0; k < 8; ++k) {
-                        uint32_t x = 0;
-                        if (k < (SBK == SB_BLOCK ? 2 : 8)) {
+                        if (SBK == SB_BLOCK)   // word h = k of [value 4 h + b][lane]
+                            wb[u][k] = (k < 2) ? ue8m0_word(vb + 128 * k, 32, mm, hh) : 0u;
+                        else                   // columns 128 (k / 4) + lane + 32 (k % 4) of [b][256]
+                            wb[u][k] = ue8m0_word(vb + 128 * (k >> 2) + 32 * (k & 3), 256, mm, hh);
+                    }
+                    if ((mm | (hh & 0x80000000u)) != 0u) {   // not all zero or normal powers of two: check each
 #pragma unroll
-                            for (int b = 0; b < KB_PER_SF; ++b) x |= ue8m0_of(vb[32 * (4 * k + b)], bad) << (8 * b);
-                        }
-                        wb[u][k] = x;
+                        for (int k = 0; k < 4; ++k)
+#pragma unroll
+                            for (int b = 0; b < KB_PER_SF; ++b) ue8m0_of(va[128 * b + 32 * k], bad);
+#pragma unroll
+                        for (int k = 0; k < (SBK == SB_BLOCK ? 2 : 8); ++k)
+#pragma unroll
+                            for (int b = 0; b < KB_PER_SF; ++b)
+                                ue8m0_of(SBK == SB_BLOCK ? vb[32 * (4 * k + b)] : vb[256 * b + 128 * (k >> 2) + 32 * (k & 3)],
+                                         bad);
                     }
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&rawempty[slot]);   // the values are in registers

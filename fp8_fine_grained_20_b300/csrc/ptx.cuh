@@ -297,6 +297,11 @@ __device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
+// 16-byte cp.async (both addresses 16-byte aligned), bypassing L1.
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread issued so far has landed;
 // the barrier's expected count must include this arrival (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

@@ -289,6 +289,47 @@ def test_mx_non_power_of_two_scale_is_reported(orc):
     assert fg.fp8_get_device_status(reset=True) == 9     # FP8_ERR_DEVICE_SCALES
 
 
+def test_mx_strided_scale_layouts(orc):
+    """Row-major A scales (stride K/128 along the rows) and per-column B scales
+    stored transposed (stride K/128 along the columns): the scale copier takes
+    one scale per copy instead of four, with the same result."""
+    qa, sa, qbt, sb = wgrad_pow2(orc, 384, 256, 384, seed=91)
+    assert sb.shape == (3, 384)
+    ref = orc.gemm_blockscaled(qa, sa, qbt, sb, orc.SB_COL128x1)
+    sa_row = gu.dev(np.ascontiguousarray(sa))              # [M, K/128], row-major
+    sb_t = gu.dev(np.ascontiguousarray(sb.T)).t()           # logical [K/128, N], strides (1, K/128)
+    C = fg.fp8_gemm_blockscaled_mx(gu.dev(qa), sa_row, gu.dev(qbt), sb_t, fg.FP8_SB_COL128x1)
+    torch.cuda.synchronize()
+    assert fg.fp8_get_device_status(reset=True) == 0
+    gu.assert_gemm_close(gu.host_bf16_as_f64(C), ref, "mx strided scale layouts")
+
+
+@pytest.mark.parametrize("bad", [1.5, np.inf, -1.0])
+def test_mx_invalid_column_scale_is_reported(orc, bad):
+    """A per-column scale that is not a power of two (x1.5), infinite or
+    negative sets FP8_ERR_DEVICE_SCALES."""
+    qa, sa, qbt, sb = wgrad_pow2(orc, 256, 128, 256, seed=47)
+    sb = sb.copy()
+    sb[1, 77] = np.float32(sb[1, 77] * np.float32(bad))
+    run_mx(qa, sa, qbt, sb, fg.FP8_SB_COL128x1)
+    assert fg.fp8_get_device_status(reset=True) == 9     # FP8_ERR_DEVICE_SCALES
+
+
+def test_mx_smallest_power_of_two_scale_is_accepted(orc):
+    """2^-127 (the fp32 subnormal 0x00400000, UE8M0 byte 0) is a valid scale
+    for A and for a B column."""
+    qa, sa, qbt, sb = wgrad_pow2(orc, 256, 128, 256, seed=48)
+    sa = sa.copy()
+    sb = sb.copy()
+    tiny = np.array([0x00400000], np.uint32).view(np.float32)[0]
+    sa[3, 0] = tiny
+    sb[1, 10] = tiny
+    ref = orc.gemm_blockscaled(qa, sa, qbt, sb, orc.SB_COL128x1)
+    C = run_mx(qa, sa, qbt, sb, fg.FP8_SB_COL128x1)
+    assert fg.fp8_get_device_status(reset=True) == 0
+    gu.assert_gemm_close(gu.host_bf16_as_f64(C), ref, "mx scale 2^-127")
+
+
 def moe_pow2(orc, counts, N, K, seed, threads=None):
     G = len(counts)
     padded = (np.asarray(counts) + 127) // 128 * 128
