@@ -813,7 +813,8 @@ def main():
     # the same step with power-of-two scales and tensor-core-applied scaling
     pow2 = None
     if not args.no_pow2:
-        pow2 = run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, device)
+        pow2 = run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, device,
+                            smi_id(torch, local))
 
     # end-to-end: pinned host inputs -> device -> step -> outputs back to pinned host
     e2e = None
@@ -882,10 +883,10 @@ def path_errors(wl, step, stream, n=2048):
     return out
 
 
-def run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, device):
+def run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, device, gpu):
     """Time the power-of-two step exactly as the main step is timed (warm-up,
-    args.steps steps between events, per-kernel events) and compare the two
-    paths' errors."""
+    args.steps steps between events, per-kernel events, clocks sampled through
+    its own timed region) and compare the two paths' errors."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -895,16 +896,22 @@ def run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, de
             for k in DeviceStep.KERNELS} for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    clocks = clock_sampler(gpu)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
     torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.time()
     with torch.cuda.stream(stream):
         t0.record(stream)
         for i in range(args.steps):
             step.run_pow2(stream, evs[i])
         t1.record(stream)
     torch.cuda.synchronize()
+    wall1 = time.time()
+    clk = clocks.stop(wall0, wall1)
     ms_step = max_over_ranks(t0.elapsed_time(t1), world, device) / args.steps
     kernels = {}
     for k in DeviceStep.KERNELS:
@@ -919,7 +926,7 @@ def run_pow2_leg(args, wl, step, stream, flops, qbytes, fp8_peak, hbm, world, de
         kernels[k] = d
     status = step.fg.fp8_get_device_status(reset=True)
     return {"ms_per_step": ms_step, "value": world * sum(flops.values()) / (ms_step * 1e-3) / 1e12,
-            "unit": UNIT, "kernels": kernels, "device_status": status,
+            "unit": UNIT, "kernels": kernels, "device_status": status, "clocks": clk,
             "errors_vs_exact_bf16_product": path_errors(wl, step, stream),
             "note": "same step, *_pow2 quantizers and the hardware block-scaled GEMMs (scales applied by "
                     "the tensor core, no FP32 promotion); not the headline"}
