@@ -422,6 +422,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 2) {
         // ------------------------------------------------ scale loader ----
+        // Scales contiguous along the rows (A) or columns (per-column B) in
+        // global memory, the usual layout, are copied four per 16-byte
+        // cp.async into the same shared-memory layout; other strides take one
+        // copy per scale.  This warp shares its scheduler with two promotion
+        // warps, so its instruction count is on their critical path.
+        const bool vec_a = p.sa_sm == 1 && (p.sa_skb & 3) == 0 && (reinterpret_cast<uintptr_t>(p.sA) & 15u) == 0;
+        const bool vec_b = SBK == SB_COL && p.sb_sn == 1 && (p.sb_skb & 3) == 0 && (p.sb_group_stride & 3) == 0 &&
+                           (reinterpret_cast<uintptr_t>(p.sB) & 15u) == 0;
         uint32_t slot = 0, sph = 0;
         bool ok = true;
         for (int t = pair; ok && t < num_tiles; t += n_pairs) {
@@ -435,17 +443,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 float* dsa = sm_sa + slot * BM;
+                if (vec_a) {
+                    const int row = r0 + 4 * lane;   // rows row .. row + 3: all in or all out (M % 128 == 0)
+                    if (row < p.M) {
+                        cp_async_16(dsa + 4 * lane, p.sA + row + static_cast<int64_t>(kb) * p.sa_skb);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < BM / 32; ++i) {
-                    const int r = lane + 32 * i;
-                    const int row = r0 + r;
-                    const float* src = (row < p.M) ? p.sA + static_cast<int64_t>(row) * p.sa_sm +
-                                                         static_cast<int64_t>(kb) * p.sa_skb
-                                                   : &g_zero_scale;
-                    cp_async_4(dsa + r, src);
+                        for (int e = 0; e < 4; ++e) cp_async_4(dsa + 4 * lane + e, &g_zero_scale);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < BM / 32; ++i) {
+                        const int r = lane + 32 * i;
+                        const int row = r0 + r;
+                        const float* src = (row < p.M) ? p.sA + static_cast<int64_t>(row) * p.sa_sm +
+                                                             static_cast<int64_t>(kb) * p.sa_skb
+                                                       : &g_zero_scale;
+                        cp_async_4(dsa + r, src);
+                    }
                 }
                 float* dsb = sm_sb + slot * BN;
-                if (SBK == SB_BLOCK) {
+                if (SBK == SB_COL && vec_b) {
+                    // columns 4 lane .. + 3 of each 128-column half: all in or all out (N % 128 == 0)
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = 128 * h + 4 * lane;
+                        const int c = tl.nb * BN + j;
+                        if (c < p.sb_cols) {
+                            cp_async_16(dsb + j, sb_base + static_cast<int64_t>(kb) * p.sb_skb + c);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) cp_async_4(dsb + j + e, &g_zero_scale);
+                        }
+                    }
+                } else if (SBK == SB_BLOCK) {
                     if (lane < BN / 128) {
                         const int c = tl.nb * (BN / 128) + lane;
                         const float* src = (c < p.sb_cols) ? sb_base + static_cast<int64_t>(kb) * p.sb_skb +
